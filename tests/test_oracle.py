@@ -1,0 +1,342 @@
+"""Pins for the oracle: values and identities fixed by the pages and by the
+mathematics, each chosen so a plausible slip (a dropped term, a wrong sign, a
+transposed operand, a wrong flattening) fails at least one test.
+
+CPU only (no GPU marker).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synthetic as S
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_rows(name):
+    rows = []
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ----------------------------------------------------------------- premix fwd
+def test_premix_hand_example():
+    """Hand-computed example from the definition (golden file)."""
+    g = {r[0]: np.array([float(t) for t in r[1:]]) for r in _read_rows("premix_hand.txt")}
+    x = g["X"].astype(np.float32).reshape(1, 1, 2, 2)
+    w = g["W"].astype(np.float32).reshape(2, 2, 2)
+    y = O.premix_fwd(x, w, P=2)
+    np.testing.assert_array_equal(y.reshape(-1), g["Y"])
+    dx = O.premix_bwd_dx(np.ones((1, 1, 4, 2), np.float32), w)
+    np.testing.assert_array_equal(dx.reshape(-1), g["DX_ONES"])
+    dw = O.premix_bwd_dw(np.ones((1, 1, 4, 2), np.float32), x, P=2)
+    np.testing.assert_array_equal(dw.reshape(-1), g["DW_ONES"])
+
+
+def test_premix_one_hot_copies_heads():
+    """W[h,p,s] = [s == sigma(h,p)] makes pseudo-head h*P+p a copy of head sigma."""
+    B, N, H, P, d = 2, 5, 5, 3, 8
+    x = S.normal((B, N, H, d), seed=1, dtype="f32")
+    sigma = lambda h, p: (3 * h + 2 * p + 1) % H
+    w = np.zeros((H, P, H), np.float32)
+    for h in range(H):
+        for p in range(P):
+            w[h, p, sigma(h, p)] = 1.0
+    y = O.premix_fwd(x, w, P)
+    for h in range(H):
+        for p in range(P):
+            np.testing.assert_array_equal(y[:, :, h * P + p, :], x[:, :, sigma(h, p), :])
+
+
+def test_premix_identity_P1():
+    x = S.normal((1, 7, 4, 16), seed=2, dtype="f32")
+    y = O.premix_fwd(x, np.eye(4, dtype=np.float32).reshape(4, 1, 4), 1)
+    np.testing.assert_array_equal(y, x)
+
+
+def test_premix_linear_in_x_and_w():
+    B, N, H, P, d = 1, 6, 4, 2, 8
+    x1 = S.normal((B, N, H, d), 3, dtype="f32")
+    x2 = S.normal((B, N, H, d), 4, dtype="f32")
+    w1 = S.premix_weight(H, P, 5, 0)
+    w2 = S.premix_weight(H, P, 6, 0)
+    a, b = np.float32(0.5), np.float32(-2.0)
+    lhs = O.premix_fwd((a * x1 + b * x2).astype(np.float32), w1, P)
+    rhs = a * O.premix_fwd(x1, w1, P) + b * O.premix_fwd(x2, w1, P)
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-6, atol=1e-6)
+    lhs = O.premix_fwd(x1, (a * w1 + b * w2).astype(np.float32), P)
+    rhs = a * O.premix_fwd(x1, w1, P) + b * O.premix_fwd(x1, w2, P)
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-6, atol=1e-6)
+
+
+# ----------------------------------------------------------------- premix bwd
+@pytest.mark.parametrize("rope", [False, True])
+def test_premix_dx_is_adjoint(rope):
+    """<dY, premix(X)> == <premix_dx(dY), X> (the chain rule, through RoPE too)."""
+    B, N, H, P, d = 2, 9, 5, 3, 16
+    x = S.normal((B, N, H, d), 7, dtype="f32")
+    dy = S.normal((B, N, H * P, d), 8, dtype="f32")
+    w = S.premix_weight(H, P, 9, 0)
+    lhs = float(np.sum(dy.astype(np.float64) * O.premix_fwd(x, w, P, rope=rope, rope_base=100.0)))
+    rhs = float(np.sum(O.premix_bwd_dx(dy, w, rope=rope, rope_base=100.0) * x.astype(np.float64)))
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+
+
+@pytest.mark.parametrize("rope", [False, True])
+def test_premix_dw_matches_difference_quotient(rope):
+    """L(W) = <dY, premix_W(X)> is linear in W, so the central difference
+    (L(W+E) - L(W-E)) / 2 is dL/dW along E exactly (up to rounding)."""
+    B, N, H, P, d = 2, 6, 3, 2, 8
+    x = S.normal((B, N, H, d), 10, dtype="f32")
+    dy = S.normal((B, N, H * P, d), 11, dtype="f32")
+    w = np.zeros((H, P, H))
+    dw = O.premix_bwd_dw(dy, x, P, rope=rope, rope_base=50.0)
+
+    def L(wm):
+        return float(np.sum(dy.astype(np.float64) *
+                            O.premix_fwd(x, wm.astype(np.float32), P, rope=rope, rope_base=50.0)))
+
+    for h in range(H):
+        for p in range(P):
+            for s in range(H):
+                E = np.zeros_like(w)
+                E[h, p, s] = 1.0
+                # L is linear, so L(W+E) - L(W-E) = L(E) - L(-E) = 2 L(E);
+                # evaluating at +-E keeps every weight exact in float32.
+                fd = (L(E) - L(-E)) / 2.0
+                assert abs(fd - dw[h, p, s]) <= 1e-9 * max(1.0, abs(fd))
+
+
+def test_premix_dw_pairs_with_forward():
+    """<dW, dWdir> == <dY, premix_dWdir(X)> for a random direction."""
+    B, N, H, P, d = 1, 11, 4, 3, 8
+    x = S.normal((B, N, H, d), 13, dtype="f32")
+    dy = S.normal((B, N, H * P, d), 14, dtype="f32")
+    dir_ = S.premix_weight(H, P, 15, 0)
+    dw = O.premix_bwd_dw(dy, x, P)
+    lhs = float(np.sum(dw * dir_.astype(np.float64)))
+    rhs = float(np.sum(dy.astype(np.float64) * O.premix_fwd(x, dir_, P)))
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+
+
+# ----------------------------------------------------------------- RoPE
+def test_rope_position_zero_is_identity_and_pairs_keep_norm():
+    x = S.normal((1, 6, 3, 16), 20, dtype="f32").astype(np.float64)
+    y = O.rope(x, base=10000.0)
+    np.testing.assert_array_equal(y[:, 0], x[:, 0])
+    half = 8
+    nx = x[..., :half] ** 2 + x[..., half:] ** 2
+    ny = y[..., :half] ** 2 + y[..., half:] ** 2
+    np.testing.assert_allclose(ny, nx, rtol=1e-12)
+    np.testing.assert_allclose(O.rope(y, base=10000.0, inverse=True), x, atol=1e-12)
+
+
+def test_rope_d2_rotates_by_position():
+    """d = 2: inv_freq_0 = base^0 = 1, so position n rotates (1, 0) by n radians."""
+    x = np.zeros((1, 4, 1, 2))
+    x[..., 0] = 1.0
+    y = O.rope(x, base=123.0)
+    for n in range(4):
+        np.testing.assert_allclose(y[0, n, 0], [math.cos(n), math.sin(n)], atol=1e-15)
+
+
+def test_rope_equals_complex_multiplication():
+    """Rotate-half RoPE == multiplying z_i = x_i + i*x_{i+d/2} by exp(i*n*base^(-2i/d))."""
+    N, d, base = 9, 12, 500.0
+    x = S.normal((1, N, 2, d), 21, dtype="f32").astype(np.float64)
+    y = O.rope(x, base=base)
+    z = x[..., : d // 2] + 1j * x[..., d // 2:]
+    theta = np.arange(N)[:, None] * base ** (-2.0 * np.arange(d // 2) / d)[None, :]
+    zr = z * np.exp(1j * theta)[None, :, None, :]
+    np.testing.assert_allclose(y[..., : d // 2], zr.real, atol=1e-12)
+    np.testing.assert_allclose(y[..., d // 2:], zr.imag, atol=1e-12)
+
+
+def test_rope_commutes_with_premix():
+    """Premix mixes heads, RoPE mixes features: R(M X) == M(R X)."""
+    B, N, H, P, d = 2, 7, 3, 2, 8
+    x = S.normal((B, N, H, d), 22, dtype="f32")
+    w = S.premix_weight(H, P, 23, 0)
+    fused = O.premix_fwd(x, w, P, rope=True, rope_base=1000.0)
+    after = O.rope(O.premix_fwd(x, w, P), base=1000.0)
+    before = O.premix_fwd(O.rope(x.astype(np.float64), base=1000.0).astype(np.float32), w, P)
+    np.testing.assert_allclose(fused, after, atol=1e-12)
+    np.testing.assert_allclose(fused, before, atol=1e-5)   # x rounded to f32 after RoPE
+
+
+# ----------------------------------------------------------------- attention
+def _qkv(Bo, Bi, N, Hh, d, seed, Nk=None):
+    Nk = N if Nk is None else Nk
+    q = S.normal((Bo, Bi, N, Hh, d), seed, 0, dtype="f32")
+    k = S.normal((Bo, Bi, Nk, Hh, d), seed, 1, dtype="f32")
+    v = S.normal((Bo, Bi, Nk, Hh, d), seed, 2, dtype="f32")
+    return q, k, v
+
+
+def _visible_count(i, N, mask, window):
+    if mask == 0:
+        return N
+    if mask == 1:
+        return i + 1
+    return min(i + 1, window)
+
+
+@pytest.mark.parametrize("mask,window", [(0, 0), (1, 0), (2, 5), (2, 1)])
+def test_attention_zero_query_is_mean_of_visible_values(mask, window):
+    q, k, v = _qkv(1, 2, 17, 2, 8, 30)
+    q[:] = 0
+    o, lse = O.attention(q, k, v, mask, window)
+    for i in range(17):
+        lo = 0 if mask == 0 else (0 if mask == 1 else max(0, i - window + 1))
+        hi = 17 if mask == 0 else i + 1
+        np.testing.assert_allclose(o[:, :, i], v[:, :, lo:hi].astype(np.float64).mean(axis=2),
+                                   atol=1e-12)
+        np.testing.assert_allclose(lse[..., i], math.log(_visible_count(i, 17, mask, window)),
+                                   atol=1e-12)
+
+
+def test_attention_window_one_returns_own_value():
+    q, k, v = _qkv(2, 1, 13, 3, 16, 31)
+    o, lse = O.attention(q, k, v, O.MASK_CAUSAL_WINDOW, 1)
+    np.testing.assert_array_equal(o, v.astype(np.float64))
+    dots = np.einsum("abnhd,abnhd->abhn", q.astype(np.float64), k.astype(np.float64))
+    np.testing.assert_allclose(lse, dots / 4.0, atol=1e-12)
+
+
+def test_attention_causal_first_row_is_first_value():
+    q, k, v = _qkv(1, 1, 9, 2, 8, 32)
+    o, _ = O.attention(q, k, v, O.MASK_CAUSAL)
+    np.testing.assert_array_equal(o[:, :, 0], v[:, :, 0].astype(np.float64))
+
+
+def test_attention_none_is_invariant_to_key_permutation():
+    q, k, v = _qkv(1, 1, 11, 2, 8, 33)
+    perm = np.random.default_rng(0).permutation(11)
+    o1, l1 = O.attention(q, k, v)
+    o2, l2 = O.attention(q, np.ascontiguousarray(k[:, :, perm]), np.ascontiguousarray(v[:, :, perm]))
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
+@pytest.mark.parametrize("mask,window,Nq,Nk", [(0, 0, 9, 14), (1, 0, 12, 12), (2, 4, 12, 12),
+                                               (2, 100, 12, 12)])
+def test_attention_matches_library_sdpa(mask, window, Nq, Nk):
+    """Brute force against torch's float64 CPU SDPA with an explicit boolean mask,
+    and lse against scipy's logsumexp of the masked scores."""
+    torch = pytest.importorskip("torch")
+    from scipy.special import logsumexp
+    Bo, Bi, Hh, d = 2, 3, 2, 8
+    q, k, v = _qkv(Bo, Bi, Nq, Hh, d, 34, Nk=Nk)
+    o, lse = O.attention(q, k, v, mask, window)
+    tq = torch.from_numpy(q.astype(np.float64)).permute(0, 1, 3, 2, 4)   # [Bo,Bi,Hh,N,d]
+    tk = torch.from_numpy(k.astype(np.float64)).permute(0, 1, 3, 2, 4)
+    tv = torch.from_numpy(v.astype(np.float64)).permute(0, 1, 3, 2, 4)
+    i = torch.arange(Nq)[:, None]
+    j = torch.arange(Nk)[None, :]
+    if mask == 0:
+        allowed = torch.ones(Nq, Nk, dtype=torch.bool)
+    elif mask == 1:
+        allowed = j <= i
+    else:
+        allowed = (j <= i) & (i - j < window)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=allowed)
+    np.testing.assert_allclose(o, ref.permute(0, 1, 3, 2, 4).numpy(), atol=1e-12)
+    scores = (tq @ tk.transpose(-1, -2)).numpy() / math.sqrt(d)
+    scores = np.where(allowed.numpy(), scores, -np.inf)
+    np.testing.assert_allclose(lse, logsumexp(scores, axis=-1), atol=1e-12)
+
+
+def test_attention_strided_views_match_dense():
+    """Hiera's (T outer, nw inner) token layout read in place equals the dense copy."""
+    B, T, nw, Hh, d = 2, 6, 3, 2, 8
+    tok = S.normal((B, T, nw, 3, Hh, d), 35, dtype="f32")        # qkv(x).view(B,T,nw,3,H,D)
+    views = [tok[:, :, :, c].transpose(0, 2, 1, 3, 4) for c in range(3)]   # [B, nw, T, H, d]
+    dense = [np.ascontiguousarray(vw) for vw in views]
+    o1, l1 = O.attention(*views)
+    o2, l2 = O.attention(*dense)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_attention_rows_match_full():
+    q, k, v = _qkv(2, 1, 21, 3, 8, 36)
+    o, lse = O.attention(q, k, v, O.MASK_CAUSAL_WINDOW, 6)
+    rows = np.array([[0, 0, 0, 0], [1, 0, 2, 20], [0, 0, 1, 7], [1, 0, 0, 5]])
+    orow, lrow = O.attention_rows(q, k, v, rows, O.MASK_CAUSAL_WINDOW, 6)
+    for r, (bo, bi, h, i) in enumerate(rows):
+        np.testing.assert_array_equal(orow[r], o[bo, bi, i, h])
+        assert lrow[r] == lse[bo, bi, h, i]
+
+
+# ----------------------------------------------------------------- tile visits
+def test_tile_matched_window_table():
+    """The page's tile-matched WSL column follows from counting 128x128 KV-tile
+    visits over H*P pseudo-heads of length N (window W = WSL + 1) against MHA
+    causal over H heads: WSL = max(N/(2P) - 1, smallest WSL matching MHA)."""
+    H, P = 20, 4
+    for N, formula, matched in [tuple(int(t) for t in r) for r in _read_rows("wsl_table.txt")]:
+        assert formula == N // (2 * P) - 1
+        mha = O.tile_visits(N, H, O.MASK_CAUSAL, 0)
+        visits = lambda wsl: O.tile_visits(N, H * P, O.MASK_CAUSAL_WINDOW, wsl + 1)
+        lo, hi = 0, N
+        while lo < hi:                      # visits are non-decreasing in WSL
+            mid = (lo + hi) // 2
+            if visits(mid) >= mha:
+                hi = mid
+            else:
+                lo = mid + 1
+        assert max(formula, lo) == matched, (N, lo, matched)
+
+
+def test_tile_visits_small_brute_force():
+    """Against a per-pair enumeration on small sizes."""
+    for N, tq, tk, mask, window in [(37, 8, 8, 1, 0), (37, 8, 4, 2, 5), (16, 4, 4, 0, 0),
+                                    (50, 16, 8, 2, 17)]:
+        count = 0
+        for a in range(0, N, tq):
+            for b in range(0, N, tk):
+                hit = False
+                for i in range(a, min(a + tq, N)):
+                    for j in range(b, min(b + tk, N)):
+                        ok = mask == 0 or (j <= i and (mask == 1 or i - j < window))
+                        hit |= ok
+                count += hit
+        assert O.tile_visits(N, 3, mask, window, tq, tk) == 3 * count
+
+
+# ----------------------------------------------------------------- gather / scatter
+def test_mu_index_map_4x4():
+    rows = [[int(t) for t in r] for r in _read_rows("mu_index_4x4.txt")]
+    x = np.arange(16, dtype=np.int32).reshape(1, 16, 1)
+    keep = np.array([[0, 1, 2, 3]], np.int32)
+    g = O.mu_gather(x, keep, 4, 4, 2, 2)
+    for r in rows:
+        assert list(g[0, r[0], :, 0]) == r[1:]
+
+
+def test_mu_scatter_inverts_gather_and_leaves_rest():
+    sh = S.MaskUnitShape(B=3, grid_h=16, grid_w=24, mu_h=4, mu_w=8, n_keep=5, C=6)
+    x = S.normal((sh.B, sh.grid_h * sh.grid_w, sh.C), 40, dtype="bf16")
+    keep = S.keep_units(sh.B, sh.n_units, sh.n_keep, 41)
+    g = O.mu_gather(x, keep, sh.grid_h, sh.grid_w, sh.mu_h, sh.mu_w)
+    canvas = np.full_like(x, 0x7FC0)                    # bf16 NaN pattern as "untouched"
+    s = O.mu_scatter(g, keep, canvas, sh.grid_h, sh.grid_w, sh.mu_h, sh.mu_w)
+    kept = s != 0x7FC0
+    np.testing.assert_array_equal(s[kept], x[kept])
+    # exactly n_keep * unit_tokens tokens per sample were written
+    assert int(kept[..., 0].sum()) == sh.B * sh.n_keep * sh.unit_tokens
+    np.testing.assert_array_equal(O.mu_gather(s, keep, sh.grid_h, sh.grid_w, sh.mu_h, sh.mu_w), g)
+
+
+def test_keep_units_sorted_unique():
+    keep = S.keep_units(128, 49, 20, 0)
+    assert keep.shape == (128, 20)
+    for row in keep:
+        assert list(row) == sorted(set(row.tolist())) and 0 <= row.min() and row.max() < 49
