@@ -1,0 +1,180 @@
+/*
+ * iha.h — C ABI of the GB300 (sm_103a) library for the Interleaved Head
+ * Attention (IHA) attention-layer hot path and Hiera mask-unit attention.
+ *
+ * Operations and where they are defined:
+ *   iha_premix_fwd / iha_premix_bwd_dx / iha_premix_bwd_dw
+ *     "IHA-CUDA: Interleaved Head Attention Kernels for Hopper GPUs",
+ *     section "Pseudo-Token Mixing (Triton Premix Kernels)": the mix
+ *     Out[h,p] = sum_s W[h,p,s] * X[s] at every (batch, position, feature),
+ *     its input gradient dX = W^T dY and its weight gradient
+ *     dW = sum over (b, n, d) of dY * X^T, with optional fused RoPE.
+ *   mha_fwd
+ *     same page, sections "Kernel Design" and "FLOP Matching": softmax
+ *     attention over the H*P pseudo-heads with a causal sliding window of
+ *     W = WSL + 1 keys; "hiera-optim 0.1.0", file
+ *     hiera_optim/attention/mask_unit.py (MaskUnitAttentionFast.forward):
+ *     unmasked attention inside each mask unit, read in Hiera's
+ *     (T outer, num_windows inner) token layout.
+ *   mu_gather / mu_scatter
+ *     "hiera-optim 0.1.0", README, "optimize(model) does two things", item 2:
+ *     boolean mask indexing of the kept mask units replaced by gather and
+ *     scatter.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named x, y, q, ... are DEVICE pointers owned by the caller.
+ *     The library allocates nothing, keeps no pointer after return and never
+ *     writes outside the output buffers named in each call.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  All argument checks happen on the host before
+ *     any launch; a failed check returns an error and launches nothing.
+ *   - IHA_ERR_CUDA means a CUDA runtime call failed (details in
+ *     iha_last_error()).  Errors that only the GPU can see (an out-of-range
+ *     keep index, an internal wait that gave up) set a device error word
+ *     that iha_device_error() reads; the offending accesses are skipped.
+ *   - Tensors are dense in their last dimension; byte strides of 16-bit
+ *     tensors must be multiples of 16 and base pointers 16-byte aligned
+ *     (IHA_ERR_ALIGNMENT otherwise).
+ */
+#ifndef IHA_H_
+#define IHA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  IHA_OK = 0,
+  IHA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad enum   */
+  IHA_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels handle   */
+  IHA_ERR_ALIGNMENT = 3,     /* base pointer or stride not 16-byte aligned  */
+  IHA_ERR_CUDA = 4           /* a CUDA runtime call or launch failed        */
+} iha_status;
+
+typedef enum { IHA_F32 = 0, IHA_BF16 = 1 } iha_dtype;
+
+typedef enum {
+  IHA_MASK_NONE = 0,           /* every key visible                          */
+  IHA_MASK_CAUSAL = 1,         /* key j visible to query i iff j <= i         */
+  IHA_MASK_CAUSAL_WINDOW = 2   /* ... and i - j < window (window = WSL + 1)   */
+} iha_mask;
+
+/* Element strides of a [B_outer, B_inner, seq, head, d] view; d is dense. */
+typedef struct {
+  int64_t b_outer;
+  int64_t b_inner;
+  int64_t seq;
+  int64_t head;
+} iha_strides;
+
+/*
+ * Premix forward ("Pseudo-Token Mixing", forward):
+ *   y[b,n,h*P+p,f] = sum_{s<H} w[h,p,s] * x[b,n,s,f]
+ * then, if rope != 0, each pseudo-head vector y[b,n,j,:] is rotated by the
+ * rotate-half RoPE of position n: for i < d/2, angle = n * rope_base^(-2i/d),
+ *   (y_i, y_{i+d/2}) <- (y_i cos - y_{i+d/2} sin, y_{i+d/2} cos + y_i sin).
+ *   x  [B, N, H, d]    dtype dt (IHA_BF16 or IHA_F32), dense
+ *   w  [H, P, H]       float32, dense
+ *   y  [B, N, H*P, d]  dtype dt, dense, must not overlap x or w
+ * Accumulation is fp32; bf16 outputs are rounded to nearest even.
+ * Requires d % 8 == 0 (bf16) or d % 4 == 0 (f32), H <= 32, H*P <= 128;
+ * rope needs d a power of two in [16, 128].
+ */
+iha_status iha_premix_fwd(const void* x, const float* w, void* y, int B, int N,
+                          int H, int P, int d, iha_dtype dt, int rope,
+                          float rope_base, void* stream);
+
+/*
+ * Premix input gradient ("Pseudo-Token Mixing", backward, dX = W^T dY):
+ *   dx[b,n,s,f] = sum_{h,p} w[h,p,s] * g[b,n,h*P+p,f]
+ * with g = dy, or g = R_n^T dy (inverse rotation) when rope != 0.
+ *   dy [B, N, H*P, d]  dtype dt;  w [H, P, H] float32;  dx [B, N, H, d] dtype dt.
+ * Same shape limits as iha_premix_fwd.
+ */
+iha_status iha_premix_bwd_dx(const void* dy, const float* w, void* dx, int B,
+                             int N, int H, int P, int d, iha_dtype dt,
+                             int rope, float rope_base, void* stream);
+
+/*
+ * Premix weight gradient ("Pseudo-Token Mixing", backward, dW = sum dY X^T):
+ *   dw[h,p,s] = sum_{b,n,f} g[b,n,h*P+p,f] * x[b,n,s,f]   (g as in dX)
+ *   dy [B, N, H*P, d] dtype dt;  x [B, N, H, d] dtype dt;
+ *   dw [H, P, H] float32, OVERWRITTEN (zeroed on `stream` first).
+ * Partial sums are reduced inside each block, then added with one float
+ * atomic per element per block, so the last bits depend on block order.
+ */
+iha_status iha_premix_bwd_dw(const void* dy, const void* x, float* dw, int B,
+                             int N, int H, int P, int d, iha_dtype dt,
+                             int rope, float rope_base, void* stream);
+
+/*
+ * Multi-head softmax attention forward over Hh heads ("Kernel Design",
+ * "FLOP Matching"; MaskUnitAttentionFast.forward):
+ *   o[i] = sum_j softmax_j(scale * <q_i, k_j> | visible(i, j)) * v_j
+ *   lse[i] = ln sum_{visible j} exp(scale * <q_i, k_j>)
+ * Views: q, o are [B_outer, B_inner, Nq, Hh, d]; k, v are
+ * [B_outer, B_inner, Nk, Hh, d]; element strides in sq, sk, sv, so.  With
+ * B_inner = num mask units and seq stride = num_units * row, Hiera's
+ * (T outer, units inner) layout is read in place.
+ *   scale     <= 0 selects 1/sqrt(d)
+ *   mask_mode IHA_MASK_NONE | IHA_MASK_CAUSAL | IHA_MASK_CAUSAL_WINDOW
+ *             (causal masks require Nq == Nk)
+ *   window    keys per query including the diagonal (W = WSL + 1), >= 1 for
+ *             IHA_MASK_CAUSAL_WINDOW, ignored otherwise
+ *   lse_out   nullable; float32 [B_outer, B_inner, Hh, Nq] dense
+ * bf16: tensor-core kernel (tcgen05, TMEM accumulators, TMA tiles), fp32
+ * softmax; needs 8 <= d <= 128, d % 8 == 0.  f32: CUDA-core kernel, fp32
+ * throughout, d <= 128.
+ */
+iha_status mha_fwd(const void* q, const void* k, const void* v, void* o,
+                   float* lse_out, int B_outer, int B_inner, int Hh, int Nq,
+                   int Nk, int d, iha_strides sq, iha_strides sk,
+                   iha_strides sv, iha_strides so, float scale,
+                   iha_mask mask_mode, int window, iha_dtype dt, void* stream);
+
+/*
+ * Mask-unit gather (README item 2, x[mask] -> gather):
+ *   out[b,k,t,:] = x[b, tok(keep[b,k], t), :]
+ * where the grid is row-major [grid_h, grid_w], mask units are mu_h x mu_w
+ * (unit u = (u / (grid_w/mu_w), u % (grid_w/mu_w))), t = ty*mu_w + tx, and
+ *   tok(u, t) = (uy*mu_h + ty) * grid_w + ux*mu_w + tx.
+ *   x    [B, grid_h*grid_w, C] elements of elem_bytes bytes, dense
+ *   keep [B, n_keep] int32 unit ids in [0, units); out-of-range ids are
+ *        skipped on the GPU and flagged in iha_device_error()
+ *   out  [B, n_keep, mu_h*mu_w, C]
+ * Bit-exact byte copy.  Requires grid_h % mu_h == 0, grid_w % mu_w == 0.
+ */
+iha_status mu_gather(const void* x, const int32_t* keep, void* out, int B,
+                     int grid_h, int grid_w, int mu_h, int mu_w, int n_keep,
+                     int C, int elem_bytes, void* stream);
+
+/*
+ * Mask-unit scatter (README item 2, x_dec[mask] = ... -> scatter), in place:
+ *   x[b, tok(keep[b,k], t), :] = src[b,k,t,:]; other tokens untouched.
+ * Same shapes and rules as mu_gather; duplicate ids within a sample race.
+ */
+iha_status mu_scatter(const void* src, const int32_t* keep, void* x, int B,
+                      int grid_h, int grid_w, int mu_h, int mu_w, int n_keep,
+                      int C, int elem_bytes, void* stream);
+
+/* Static description of a status code. */
+const char* iha_status_string(iha_status status);
+
+/* Detail of the last error returned on the calling host thread ("" if none). */
+const char* iha_last_error(void);
+
+/*
+ * Device error word of the current device: 0 if no kernel has flagged an
+ * error, else a code (1 = out-of-range keep index, 2 = a bounded internal
+ * wait gave up).  Synchronises the device; clears the word if clear != 0.
+ * Returns -1 if the word cannot be read.
+ */
+int iha_device_error(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IHA_H_ */

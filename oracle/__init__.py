@@ -40,7 +40,7 @@ def lib() -> C.CDLL:
         L.oracle_num_threads.restype = C.c_int
         L.oracle_rope.argtypes = [dp, dp, l, l, l, l, d, i]
         for name in ("oracle_premix_fwd", "oracle_premix_bwd_dx"):
-            getattr(L, name).argtypes = [fp, fp, dp, l, l, l, l, l, i, d]
+            getattr(L, name).argtypes = [fp, fp, dp, l, l, l, l, l, i, d, l]
         L.oracle_premix_bwd_dw.argtypes = [fp, fp, dp, l, l, l, l, l, i, d]
         L.oracle_attention.argtypes = [fp, fp, fp, dp, dp, l, l, l, l, l, l,
                                        lp, lp, lp, d, i, l]
@@ -75,19 +75,22 @@ MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW = 0, 1, 2
 
 # ------------------------------------------------------------------ premix
 def premix_fwd(x: np.ndarray, w: np.ndarray, P: int, rope: bool = False,
-               rope_base: float = 10000.0) -> np.ndarray:
-    """Y[B,N,H*P,d] (float64) from X[B,N,H,d] and W[H,P,H]."""
+               rope_base: float = 10000.0, pos0: int = 0) -> np.ndarray:
+    """Y[B,N,H*P,d] (float64) from X[B,N,H,d] and W[H,P,H].
+
+    pos0: RoPE position of the first row (for a window of a longer sequence).
+    """
     B, N, H, d = x.shape
     xf, wf = _as_f32(x), _as_f32(w)
     assert wf.shape == (H, P, H)
     y = np.empty((B, N, H * P, d), dtype=np.float64)
     lib().oracle_premix_fwd(_p(xf, C.c_float), _p(wf, C.c_float), _p(y, C.c_double),
-                            B, N, H, P, d, int(rope), float(rope_base))
+                            B, N, H, P, d, int(rope), float(rope_base), int(pos0))
     return y
 
 
 def premix_bwd_dx(dy: np.ndarray, w: np.ndarray, rope: bool = False,
-                  rope_base: float = 10000.0) -> np.ndarray:
+                  rope_base: float = 10000.0, pos0: int = 0) -> np.ndarray:
     """dX[B,N,H,d] (float64) from dY[B,N,H*P,d] and W[H,P,H]."""
     B, N, HP, d = dy.shape
     H, P, _ = w.shape
@@ -95,7 +98,7 @@ def premix_bwd_dx(dy: np.ndarray, w: np.ndarray, rope: bool = False,
     gf, wf = _as_f32(dy), _as_f32(w)
     dx = np.empty((B, N, H, d), dtype=np.float64)
     lib().oracle_premix_bwd_dx(_p(gf, C.c_float), _p(wf, C.c_float), _p(dx, C.c_double),
-                               B, N, H, P, d, int(rope), float(rope_base))
+                               B, N, H, P, d, int(rope), float(rope_base), int(pos0))
     return dx
 
 

@@ -86,10 +86,12 @@ void oracle_rope(const double* x, double* y, long B, long N, long heads,
 /* ------------------------------------------------------------------------ */
 /* Premix forward: Y[b,n,h*P+p,f] = sum_s W[h,p,s] * X[b,n,s,f]              */
 /* then, if rope != 0, each pseudo-head vector Y[b,n,j,:] is rotated by R_n.  */
+/* The input may be a window of positions: row n of the input sits at        */
+/* position pos0 + n (pos0 = 0 for whole sequences).                         */
 /* ------------------------------------------------------------------------ */
 void oracle_premix_fwd(const float* x, const float* w, double* y, long B,
                        long N, long H, long P, long d, int rope,
-                       double rope_base) {
+                       double rope_base, long pos0) {
   long HP = H * P;
 #pragma omp parallel for schedule(static)
   for (long bn = 0; bn < B * N; ++bn) {
@@ -106,7 +108,7 @@ void oracle_premix_fwd(const float* x, const float* w, double* y, long B,
     if (rope) {
       double tmp[HP * d];
       memcpy(tmp, yt, sizeof(double) * HP * d);
-      rope_token(tmp, yt, HP, d, bn % N, rope_base, 0);
+      rope_token(tmp, yt, HP, d, pos0 + bn % N, rope_base, 0);
     }
   }
 }
@@ -118,7 +120,7 @@ void oracle_premix_fwd(const float* x, const float* w, double* y, long B,
 /* ------------------------------------------------------------------------ */
 void oracle_premix_bwd_dx(const float* dy, const float* w, double* dx, long B,
                           long N, long H, long P, long d, int rope,
-                          double rope_base) {
+                          double rope_base, long pos0) {
   long HP = H * P;
 #pragma omp parallel for schedule(static)
   for (long bn = 0; bn < B * N; ++bn) {
@@ -127,7 +129,7 @@ void oracle_premix_bwd_dx(const float* dy, const float* w, double* dx, long B,
     if (rope) {
       double tmp[HP * d];
       memcpy(tmp, g, sizeof(double) * HP * d);
-      rope_token(tmp, g, HP, d, bn % N, rope_base, 1);
+      rope_token(tmp, g, HP, d, pos0 + bn % N, rope_base, 1);
     }
     double* out = dx + bn * H * d;
     for (long s = 0; s < H; ++s)

@@ -1,0 +1,110 @@
+"""CPU tests of the C ABI: the library loads, exports every function that
+include/iha.h declares, and rejects bad arguments on the host before any
+launch (no GPU is touched: every call here fails validation)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import transformer_attention_iha_gb300 as T
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    T.build()
+    return T.lib()
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+    assert set(T.SYMBOLS) <= set(names)
+
+
+def test_status_strings(L):
+    for s in range(5):
+        assert L.iha_status_string(s)
+    assert L.iha_status_string(99) == b"unknown status"
+
+
+FAKE = C.c_void_p(0x10000)       # never dereferenced: every call below fails validation
+MISALIGNED = C.c_void_p(0x10008)
+
+
+def _err(L):
+    return L.iha_last_error().decode()
+
+
+def test_premix_validation(L):
+    assert L.iha_premix_fwd(None, FAKE, FAKE, 1, 8, 4, 2, 32, T.BF16, 0, 1e4, None) == 1
+    assert L.iha_premix_fwd(FAKE, FAKE, FAKE, 0, 8, 4, 2, 32, T.BF16, 0, 1e4, None) == 1
+    assert L.iha_premix_fwd(FAKE, FAKE, FAKE, 1, 8, 4, 2, 32, 7, 0, 1e4, None) == 1
+    assert L.iha_premix_fwd(FAKE, FAKE, FAKE, 1, 8, 33, 1, 32, T.BF16, 0, 1e4, None) == 2
+    assert L.iha_premix_fwd(FAKE, FAKE, FAKE, 1, 8, 20, 7, 32, T.BF16, 0, 1e4, None) == 2
+    assert L.iha_premix_fwd(FAKE, FAKE, FAKE, 1, 8, 4, 2, 12, T.BF16, 0, 1e4, None) == 2
+    assert L.iha_premix_fwd(FAKE, FAKE, FAKE, 1, 8, 4, 2, 96, T.BF16, 1, 1e4, None) == 2
+    assert "RoPE" in _err(L)
+    assert L.iha_premix_fwd(FAKE, FAKE, FAKE, 1, 8, 4, 2, 64, T.BF16, 1, -1.0, None) == 1
+    assert L.iha_premix_fwd(MISALIGNED, FAKE, FAKE, 1, 8, 4, 2, 32, T.BF16, 0, 1e4, None) == 3
+    assert L.iha_premix_bwd_dx(FAKE, None, FAKE, 1, 8, 4, 2, 32, T.BF16, 0, 1e4, None) == 1
+    assert L.iha_premix_bwd_dw(FAKE, FAKE, MISALIGNED, 1, 8, 4, 2, 32, T.BF16, 0, 1e4, None) == 3
+    # output overlapping an input
+    assert L.iha_premix_fwd(FAKE, FAKE, FAKE, 1, 8, 4, 2, 32, T.BF16, 0, 1e4, None) == 1
+    assert "overlap" in _err(L)
+
+
+def _s(b_outer, b_inner, seq, head):
+    return T.Strides(b_outer, b_inner, seq, head)
+
+
+def test_attention_validation(L):
+    s = _s(8 * 64 * 2, 8 * 64 * 2, 64 * 2, 64)
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE)
+
+    def call(q=FAKE, o=FAKE, Bo=1, Bi=1, Hh=2, Nq=8, Nk=8, d=64, sq=s, mask=0, window=0,
+             dt=T.BF16):
+        return L.mha_fwd(q, FAKE, FAKE, o, None, Bo, Bi, Hh, Nq, Nk, d, sq, s, s, s, 0.0,
+                         mask, window, dt, None)
+
+    assert call(q=None) == 1
+    assert call(Nq=0) == 1
+    assert call(mask=5) == 1
+    assert call(mask=2, window=0) == 1
+    assert call(mask=1, Nk=9) == 2
+    assert call(d=256) == 2
+    assert call(d=12) == 2
+    assert call(q=MISALIGNED) == 3
+    assert call(sq=_s(8 * 64 * 2, 8 * 64 * 2, 68 * 2, 68)) == 3
+    assert call(Bo=300, Bi=300) == 2
+
+
+def test_mask_unit_validation(L):
+    assert L.mu_gather(FAKE, FAKE, FAKE, 1, 10, 10, 3, 3, 1, 8, 2, None) == 1   # 10 % 3
+    assert L.mu_gather(FAKE, FAKE, FAKE, 1, 8, 8, 4, 4, 5, 8, 2, None) == 1     # 5 > 4 units
+    assert L.mu_scatter(None, FAKE, FAKE, 1, 8, 8, 4, 4, 1, 8, 2, None) == 1
+    assert L.mu_scatter(FAKE, FAKE, FAKE, 1, 8, 8, 4, 4, 1, 8, 2, None) == 1    # aliasing
+
+
+def test_python_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
+    """The product path fails loudly when the extension is missing."""
+    import importlib
+    mod = importlib.import_module("transformer_attention_iha_gb300")
+    monkeypatch.setattr(mod, "_lib", None)
+    monkeypatch.setattr(mod._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        mod.lib()

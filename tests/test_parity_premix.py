@@ -1,0 +1,142 @@
+"""GPU parity: premix forward / input gradient / weight gradient vs the oracle.
+
+Small shapes run the whole oracle (several blocks and a ragged tail); the
+LLaMA-2.4B layer shape (B=1, N=8192, H=20, P=4, d=128) checks sampled token
+windows for the forward and input gradient and the full weight gradient; the
+long-context shape (B=2, N=16384) checks RoPE at late positions.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import synthetic as S
+from helpers import (abs_bits, assert_bf16_close, assert_dw_close, assert_f32_close, to_dev,
+                     to_f64)
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [  # (B, N, H, P, d)
+    (2, 37, 20, 4, 128),
+    (1, 5, 4, 2, 32),
+    (3, 9, 3, 3, 64),
+    (1, 33, 7, 5, 96),
+    (2, 17, 32, 4, 16),
+    (1, 3, 1, 1, 8),
+]
+
+
+@pytest.fixture(scope="module")
+def T():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import transformer_attention_iha_gb300 as T
+    T.lib()
+    return T
+
+
+def _inputs(B, N, H, P, d, seed, dtype="bf16"):
+    x = S.normal((B, N, H, d), seed, 0, dtype=dtype)
+    dy = S.normal((B, N, H * P, d), seed, 1, dtype=dtype)
+    w = S.premix_weight(H, P, seed, 2)
+    return x, dy, w
+
+
+def _rope_ok(d):
+    return d >= 16 and d <= 128 and (d & (d - 1)) == 0
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("rope", [False, True])
+def test_premix_bf16_small(T, shape, rope):
+    B, N, H, P, d = shape
+    if rope and not _rope_ok(d):
+        pytest.skip("RoPE needs d a power of two")
+    x, dy, w = _inputs(B, N, H, P, d, seed=11 + d)
+    base = 100.0
+    y = T.premix_fwd(to_dev(x), to_dev(w), P, rope=rope, rope_base=base)
+    assert_bf16_close(to_f64(y), O.premix_fwd(x, w, P, rope=rope, rope_base=base), "fwd")
+    dx = T.premix_bwd_dx(to_dev(dy), to_dev(w), rope=rope, rope_base=base)
+    assert_bf16_close(to_f64(dx), O.premix_bwd_dx(dy, w, rope=rope, rope_base=base), "dx")
+    dw = T.premix_bwd_dw(to_dev(dy), to_dev(x), P, rope=rope, rope_base=base)
+    absum = O.premix_bwd_dw(abs_bits(dy), abs_bits(x), P) * (2.0 if rope else 1.0)
+    assert_dw_close(to_f64(dw), O.premix_bwd_dw(dy, x, P, rope=rope, rope_base=base), absum, "dw")
+
+
+@pytest.mark.parametrize("rope", [False, True])
+def test_premix_f32_tiny_layer(T, rope):
+    """fp32 path at the tiny-layer shape (B=1, N=128, H=4, P=2, d=32): 1e-5."""
+    sh = S.TINY
+    x, dy, w = _inputs(sh.B, sh.N, sh.H, sh.P, sh.d, seed=0, dtype="f32")
+    y = T.premix_fwd(to_dev(x), to_dev(w), sh.P, rope=rope)
+    assert_f32_close(to_f64(y), O.premix_fwd(x, w, sh.P, rope=rope), "fwd f32")
+    dx = T.premix_bwd_dx(to_dev(dy), to_dev(w), rope=rope)
+    assert_f32_close(to_f64(dx), O.premix_bwd_dx(dy, w, rope=rope), "dx f32")
+    dw = T.premix_bwd_dw(to_dev(dy), to_dev(x), sh.P, rope=rope)
+    r = O.premix_bwd_dw(dy, x, sh.P, rope=rope)
+    # fp32 reduction over B*N*d = 4096 products of N(0,1) values
+    assert_f32_close(to_f64(dw), r, "dw f32", tol=1e-5 * max(1.0, float(np.abs(r).max())))
+
+
+def test_premix_llama_shape_sampled(T):
+    """B=1, N=8192, H=20, P=4, d=128 (the bench shape): token windows at the
+    start, middle and end for fwd / dx; the full dW."""
+    sh = S.LLAMA_PREMIX
+    x, dy, w = _inputs(sh.B, sh.N, sh.H, sh.P, sh.d, seed=0)
+    y = to_f64(T.premix_fwd(to_dev(x), to_dev(w), sh.P))
+    dx = to_f64(T.premix_bwd_dx(to_dev(dy), to_dev(w)))
+    for n0 in (0, 4093, sh.N - 131):
+        sl = slice(n0, n0 + 131)
+        assert_bf16_close(y[:, sl], O.premix_fwd(x[:, sl], w, sh.P), f"fwd@{n0}")
+        assert_bf16_close(dx[:, sl], O.premix_bwd_dx(dy[:, sl], w), f"dx@{n0}")
+    dw = to_f64(T.premix_bwd_dw(to_dev(dy), to_dev(x), sh.P))
+    absum = O.premix_bwd_dw(abs_bits(dy), abs_bits(x), sh.P)
+    assert_dw_close(dw, O.premix_bwd_dw(dy, x, sh.P), absum, "dw full")
+
+
+def test_premix_long_context_rope_sampled(T):
+    """B=2, N=16384 with RoPE (base 10000): windows near the end of each
+    sequence, where angles are largest."""
+    sh = S.LONG_CTX
+    x = S.normal((sh.B, sh.N, sh.H, sh.d), 5, 0)
+    w = S.premix_weight(sh.H, sh.P, 5, 1)
+    y = to_f64(T.premix_fwd(to_dev(x), to_dev(w), sh.P, rope=True, rope_base=S.ROPE_BASE))
+    for n0 in (0, 9001, sh.N - 67):
+        sl = slice(n0, n0 + 67)
+        ref = O.premix_fwd(x[:, sl], w, sh.P, rope=True, rope_base=S.ROPE_BASE, pos0=n0)
+        assert_bf16_close(y[:, sl], ref, f"fwd rope@{n0}")
+    dy = S.normal((sh.B, sh.N, sh.HP, sh.d), 5, 2)
+    dx = to_f64(T.premix_bwd_dx(to_dev(dy), to_dev(w), rope=True, rope_base=S.ROPE_BASE))
+    for n0 in (0, sh.N - 67):
+        sl = slice(n0, n0 + 67)
+        ref = O.premix_bwd_dx(dy[:, sl], w, rope=True, rope_base=S.ROPE_BASE, pos0=n0)
+        assert_bf16_close(dx[:, sl], ref, f"dx rope@{n0}")
+
+
+def test_premix_one_hot_copies_are_bit_exact(T):
+    """One-hot W makes every pseudo-head an exact copy of a source head."""
+    B, N, H, P, d = 2, 19, 5, 3, 64
+    x = S.normal((B, N, H, d), 3, 0)
+    w = np.zeros((H, P, H), np.float32)
+    for h in range(H):
+        for p in range(P):
+            w[h, p, (2 * h + p) % H] = 1.0
+    y = T.premix_fwd(to_dev(x), to_dev(w), P)
+    yb = y.view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+    for h in range(H):
+        for p in range(P):
+            np.testing.assert_array_equal(yb[:, :, h * P + p], x[:, :, (2 * h + p) % H])
+
+
+def test_premix_rejects_bad_args(T):
+    import torch
+    x = torch.zeros((1, 4, 3, 10), dtype=torch.bfloat16, device="cuda")   # d % 8 != 0
+    w = torch.zeros((3, 2, 3), dtype=torch.float32, device="cuda")
+    with pytest.raises(T.IHAError) as e:
+        T.premix_fwd(x, w, 2)
+    assert e.value.status == 2
+    x = torch.zeros((1, 4, 33, 16), dtype=torch.bfloat16, device="cuda")  # H > 32
+    w = torch.zeros((33, 1, 33), dtype=torch.float32, device="cuda")
+    with pytest.raises(T.IHAError):
+        T.premix_fwd(x, w, 1)
+    assert T.device_error() == 0

@@ -1,0 +1,234 @@
+"""GB300 (sm_103a) library for the Interleaved Head Attention hot path.
+
+Thin ctypes binding over ``libiha.so``: argument marshalling only.  Every
+step runs in the library's CUDA kernels; there is no CPU or PyTorch fallback.
+If the library is missing, ``lib()`` raises instead of degrading.
+
+Entry points (same names as the C ABI in include/iha.h):
+  premix_fwd, premix_bwd_dx, premix_bwd_dw   -- "IHA-CUDA", section
+      "Pseudo-Token Mixing (Triton Premix Kernels)"
+  mha_fwd                                   -- "IHA-CUDA", sections "Kernel
+      Design" and "FLOP Matching"; hiera-optim MaskUnitAttentionFast.forward
+  mu_gather, mu_scatter                     -- "hiera-optim 0.1.0", README,
+      item 2 of what optimize(model) does
+PyTorch supplies device memory and the current stream only.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+from . import _build
+
+__all__ = ["build", "lib", "premix_fwd", "premix_bwd_dx", "premix_bwd_dw", "mha_fwd",
+           "mu_gather", "mu_scatter", "device_error", "IHAError", "Strides", "MASK_NONE",
+           "MASK_CAUSAL", "MASK_CAUSAL_WINDOW", "F32", "BF16"]
+
+IHA_OK, IHA_ERR_INVALID_ARG, IHA_ERR_UNSUPPORTED, IHA_ERR_ALIGNMENT, IHA_ERR_CUDA = range(5)
+F32, BF16 = 0, 1
+MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW = 0, 1, 2
+
+SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "mha_fwd", "mu_gather",
+           "mu_scatter", "iha_status_string", "iha_last_error", "iha_device_error")
+
+
+class IHAError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: status {status} ({detail})")
+        self.status = status
+
+
+class Strides(C.Structure):
+    """Element strides (b_outer, b_inner, seq, head) of a [Bo, Bi, N, Hh, d] view."""
+    _fields_ = [("b_outer", C.c_int64), ("b_inner", C.c_int64), ("seq", C.c_int64),
+                ("head", C.c_int64)]
+
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libiha.so for sm_103a (in-tree)."""
+    return _build.build(force=force)
+
+
+def lib() -> C.CDLL:
+    """The loaded C-ABI library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"{_build.LIB} is missing: run transformer_attention_iha_gb300.build()")
+    L = C.CDLL(_build.LIB)
+    vp, i, f = C.c_void_p, C.c_int, C.c_float
+    L.iha_premix_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    L.iha_premix_bwd_dx.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    L.iha_premix_bwd_dw.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    L.mha_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, Strides, Strides, Strides,
+                          Strides, f, i, i, i, vp]
+    L.mu_gather.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
+    L.mu_scatter.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
+    for name in ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "mha_fwd",
+                 "mu_gather", "mu_scatter"):
+        getattr(L, name).restype = C.c_int
+    L.iha_status_string.argtypes = [i]
+    L.iha_status_string.restype = C.c_char_p
+    L.iha_last_error.argtypes = []
+    L.iha_last_error.restype = C.c_char_p
+    L.iha_device_error.argtypes = [i]
+    L.iha_device_error.restype = C.c_int
+    _lib = L
+    return L
+
+
+def check(status: int, where: str) -> None:
+    if status != IHA_OK:
+        L = lib()
+        detail = L.iha_last_error().decode() or L.iha_status_string(status).decode()
+        raise IHAError(status, where, detail)
+
+
+def device_error(clear: bool = True) -> int:
+    """Device error word (0 = none); synchronises the device."""
+    return int(lib().iha_device_error(int(clear)))
+
+
+# ---------------------------------------------------------------- torch helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _dt(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return C.c_void_p(t.data_ptr())
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+
+
+# ---------------------------------------------------------------- premix
+def premix_fwd(x, w, P: int, rope: bool = False, rope_base: float = 10000.0, out=None,
+               stream=None):
+    """Y[B,N,H*P,d] = premix of X[B,N,H,d] with W[H,P,H] (fp32), optional RoPE."""
+    torch = _torch()
+    _need_cuda(x, w)
+    B, N, H, d = x.shape
+    if out is None:
+        out = torch.empty((B, N, H * P, d), dtype=x.dtype, device=x.device)
+    check(lib().iha_premix_fwd(_ptr(x), _ptr(w), _ptr(out), B, N, H, P, d, _dt(x), int(rope),
+                               float(rope_base), _stream(stream)), "iha_premix_fwd")
+    return out
+
+
+def premix_bwd_dx(dy, w, rope: bool = False, rope_base: float = 10000.0, out=None,
+                  stream=None):
+    """dX[B,N,H,d] = W^T dY (with the inverse RoPE when rope)."""
+    torch = _torch()
+    _need_cuda(dy, w)
+    B, N, HP, d = dy.shape
+    H, P, _ = w.shape
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=dy.dtype, device=dy.device)
+    check(lib().iha_premix_bwd_dx(_ptr(dy), _ptr(w), _ptr(out), B, N, H, P, d, _dt(dy),
+                                  int(rope), float(rope_base), _stream(stream)),
+          "iha_premix_bwd_dx")
+    return out
+
+
+def premix_bwd_dw(dy, x, P: int, rope: bool = False, rope_base: float = 10000.0, out=None,
+                  stream=None):
+    """dW[H,P,H] (fp32, overwritten) = sum over tokens and features of dY X^T."""
+    torch = _torch()
+    _need_cuda(dy, x)
+    B, N, H, d = x.shape
+    if out is None:
+        out = torch.empty((H, P, H), dtype=torch.float32, device=x.device)
+    check(lib().iha_premix_bwd_dw(_ptr(dy), _ptr(x), _ptr(out), B, N, H, P, d, _dt(x),
+                                  int(rope), float(rope_base), _stream(stream)),
+          "iha_premix_bwd_dw")
+    return out
+
+
+# ---------------------------------------------------------------- attention
+def _as5(t):
+    """View a [B, N, Hh, d] or [Bo, Bi, N, Hh, d] tensor as 5-D (no copy)."""
+    if t.dim() == 4:
+        return t.unsqueeze(1)
+    if t.dim() == 5:
+        return t
+    raise ValueError("attention tensors must be [B,N,Hh,d] or [Bo,Bi,N,Hh,d]")
+
+
+def _strides(t5) -> Strides:
+    s = t5.stride()
+    if s[4] != 1:
+        raise ValueError("the head dimension must be dense")
+    return Strides(s[0], s[1], s[2], s[3])
+
+
+def mha_fwd(q, k, v, mask: int = MASK_NONE, window: int = 0, scale: float = 0.0, out=None,
+            lse=None, return_lse: bool = False, stream=None):
+    """Softmax attention over [B,N,Hh,d] or [Bo,Bi,N,Hh,d] views (strided allowed).
+
+    Returns O shaped like q (dense unless `out` is given); with return_lse,
+    also lse [Bo, Bi, Hh, Nq] fp32 (natural log, scale included).
+    """
+    torch = _torch()
+    _need_cuda(q, k, v)
+    q5, k5, v5 = _as5(q), _as5(k), _as5(v)
+    Bo, Bi, Nq, Hh, d = q5.shape
+    Nk = k5.shape[2]
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    o5 = _as5(out)
+    if lse is None and return_lse:
+        lse = torch.empty((Bo, Bi, Hh, Nq), dtype=torch.float32, device=q.device)
+    check(lib().mha_fwd(_ptr(q5), _ptr(k5), _ptr(v5), _ptr(o5),
+                        C.c_void_p(lse.data_ptr() if lse is not None else 0), Bo, Bi, Hh, Nq,
+                        Nk, d, _strides(q5), _strides(k5), _strides(v5), _strides(o5),
+                        float(scale), int(mask), int(window), _dt(q), _stream(stream)),
+          "mha_fwd")
+    return (out, lse) if return_lse else out
+
+
+# ---------------------------------------------------------------- gather / scatter
+def mu_gather(x, keep, grid_h: int, grid_w: int, mu_h: int, mu_w: int, out=None, stream=None):
+    """x [B, grid_h*grid_w, C] -> [B, n_keep, mu_h*mu_w, C] (bit-exact copy)."""
+    torch = _torch()
+    _need_cuda(x, keep)
+    B, G, Cc = x.shape
+    n_keep = keep.shape[1]
+    if out is None:
+        out = torch.empty((B, n_keep, mu_h * mu_w, Cc), dtype=x.dtype, device=x.device)
+    check(lib().mu_gather(_ptr(x), _ptr(keep), _ptr(out), B, grid_h, grid_w, mu_h, mu_w, n_keep,
+                          Cc, x.element_size(), _stream(stream)), "mu_gather")
+    return out
+
+
+def mu_scatter(src, keep, x, grid_h: int, grid_w: int, mu_h: int, mu_w: int, stream=None):
+    """In place: x[b, tok(keep[b,k], t), :] = src[b, k, t, :]."""
+    _need_cuda(src, keep, x)
+    B, G, Cc = x.shape
+    n_keep = keep.shape[1]
+    check(lib().mu_scatter(_ptr(src), _ptr(keep), _ptr(x), B, grid_h, grid_w, mu_h, mu_w, n_keep,
+                           Cc, x.element_size(), _stream(stream)), "mu_scatter")
+    return x
