@@ -4,8 +4,9 @@
 One step = one pass of every hot-path operation over one batch of seeded
 synthetic inputs, each at its workload's shape:
   premix   LLaMA-2.4B layer shape B=1, N=8192, H=20, P=4, d=128:
-           forward for Q and K (fused RoPE, base 10000) and V, input gradient
-           for Q, K (inverse RoPE) and V, weight gradient for Q, K, V;
+           forward for Q and K (fused RoPE, base 10000) and V; backward (input
+           gradient with inverse RoPE for Q, K, and weight gradient) for Q, K, V,
+           both gradients from one pass over dY;
   attention 80 pseudo-heads, N=4096, d=128, causal window W=1024, fp32 LSE;
   Hiera    MAE stage 1, B=128, 56x56 tokens, 8x8 units, 20 kept, C=d=96:
            gather, attention inside each unit, scatter.
@@ -69,10 +70,8 @@ def op_table():
     ops = []
     for t in ("q", "k", "v"):
         ops.append((f"premix_fwd_{t}", "premix", x_b + y_b + w_b, premix_flops))
-    for t in ("q", "k", "v"):
-        ops.append((f"premix_dx_{t}", "premix", y_b + x_b + w_b, premix_flops))
-    for t in ("q", "k", "v"):
-        ops.append((f"premix_dw_{t}", "premix", y_b + x_b + w_b, premix_flops))
+    for t in ("q", "k", "v"):   # dX and dW from one read of dY and X
+        ops.append((f"premix_bwd_{t}", "premix", y_b + 2 * x_b + 2 * w_b, 2 * premix_flops))
     aw = S.LLAMA_WINDOW
     W = S.WINDOW_KEYS
     pairs = sum(min(i + 1, W) for i in range(aw.N))
@@ -88,7 +87,7 @@ def op_table():
     return ops
 
 
-LAUNCHES_PER_STEP = 3 + 3 + 3 * 2 + 1 + 3   # premix fwd/dx, dw (zero + reduce), attention, MU x3
+LAUNCHES_PER_STEP = 3 + 3 * 2 + 1 + 3   # premix fwd, bwd (zero dW + kernel), attention, MU x3
 
 
 def host_inputs(seed: int):
@@ -158,13 +157,8 @@ class Step:
             k += 1
             mark(k)
         for t in "qkv":
-            T.premix_bwd_dx(i[f"dy_{t}"], i[f"w_{t}"], rope=(t != "v"), rope_base=S.ROPE_BASE,
-                            out=self.dx[t])
-            k += 1
-            mark(k)
-        for t in "qkv":
-            T.premix_bwd_dw(i[f"dy_{t}"], i[f"x_{t}"], pm.P, rope=(t != "v"),
-                            rope_base=S.ROPE_BASE, out=self.dw[t])
+            T.premix_bwd(i[f"dy_{t}"], i[f"x_{t}"], i[f"w_{t}"], rope=(t != "v"),
+                         rope_base=S.ROPE_BASE, dx=self.dx[t], dw=self.dw[t])
             k += 1
             mark(k)
         T.mha_fwd(i["a_q"], i["a_k"], i["a_v"], mask=T.MASK_CAUSAL_WINDOW, window=S.WINDOW_KEYS,
@@ -358,7 +352,7 @@ def gpu_arm(args, rank, world, local_rank):
         "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, W ~ N(0,1/H) fp32)",
-        "config": {"workload": "IHA hot-path step: premix fwd(+RoPE)/dX/dW for Q,K,V at "
+        "config": {"workload": "IHA hot-path step: premix fwd(+RoPE) and fused dX+dW for Q,K,V at "
                                "B=1,N=8192,H=20,P=4,d=128; causal-window attention 80 heads "
                                "N=4096 d=128 W=1024; Hiera-Base MAE stage-1 gather + mask-unit "
                                "attention (2560 units x 64 tokens, d=96) + scatter",

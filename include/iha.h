@@ -110,6 +110,19 @@ iha_status iha_premix_bwd_dw(const void* dy, const void* x, float* dw, int B,
                              int rope, float rope_base, void* stream);
 
 /*
+ * Premix backward, both gradients in one pass over dY ("Pseudo-Token Mixing",
+ * backward): dx as iha_premix_bwd_dx and dw as iha_premix_bwd_dw, from one
+ * read of dy (and x).  Algorithmic traffic per token: dY + X + dX instead of
+ * 2 dY + X + dX for the two separate calls.
+ *   dy [B, N, H*P, d], x [B, N, H, d], dx [B, N, H, d] (dtype dt);
+ *   w [H, P, H] float32;  dw [H, P, H] float32, OVERWRITTEN.
+ * Same shape limits as iha_premix_fwd; outputs must not overlap any input.
+ */
+iha_status iha_premix_bwd(const void* dy, const void* x, const float* w, void* dx,
+                          float* dw, int B, int N, int H, int P, int d,
+                          iha_dtype dt, int rope, float rope_base, void* stream);
+
+/*
  * Multi-head softmax attention forward over Hh heads ("Kernel Design",
  * "FLOP Matching"; MaskUnitAttentionFast.forward):
  *   o[i] = sum_j softmax_j(scale * <q_i, k_j> | visible(i, j)) * v_j

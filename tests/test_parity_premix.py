@@ -60,7 +60,12 @@ def test_premix_bf16_small(T, shape, rope):
     assert_bf16_close(to_f64(dx), O.premix_bwd_dx(dy, w, rope=rope, rope_base=base), "dx")
     dw = T.premix_bwd_dw(to_dev(dy), to_dev(x), P, rope=rope, rope_base=base)
     absum = O.premix_bwd_dw(abs_bits(dy), abs_bits(x), P) * (2.0 if rope else 1.0)
-    assert_dw_close(to_f64(dw), O.premix_bwd_dw(dy, x, P, rope=rope, rope_base=base), absum, "dw")
+    rdw = O.premix_bwd_dw(dy, x, P, rope=rope, rope_base=base)
+    assert_dw_close(to_f64(dw), rdw, absum, "dw")
+    # both gradients from one pass over dY
+    dx2, dw2 = T.premix_bwd(to_dev(dy), to_dev(x), to_dev(w), rope=rope, rope_base=base)
+    assert_bf16_close(to_f64(dx2), O.premix_bwd_dx(dy, w, rope=rope, rope_base=base), "fused dx")
+    assert_dw_close(to_f64(dw2), rdw, absum, "fused dw")
 
 
 @pytest.mark.parametrize("rope", [False, True])
@@ -91,7 +96,14 @@ def test_premix_llama_shape_sampled(T):
         assert_bf16_close(dx[:, sl], O.premix_bwd_dx(dy[:, sl], w), f"dx@{n0}")
     dw = to_f64(T.premix_bwd_dw(to_dev(dy), to_dev(x), sh.P))
     absum = O.premix_bwd_dw(abs_bits(dy), abs_bits(x), sh.P)
-    assert_dw_close(dw, O.premix_bwd_dw(dy, x, sh.P), absum, "dw full")
+    rdw = O.premix_bwd_dw(dy, x, sh.P)
+    assert_dw_close(dw, rdw, absum, "dw full")
+    dx2, dw2 = T.premix_bwd(to_dev(dy), to_dev(x), to_dev(w))
+    dx2 = to_f64(dx2)
+    for n0 in (0, sh.N - 131):
+        sl = slice(n0, n0 + 131)
+        assert_bf16_close(dx2[:, sl], O.premix_bwd_dx(dy[:, sl], w), f"fused dx@{n0}")
+    assert_dw_close(to_f64(dw2), rdw, absum, "fused dw full")
 
 
 def test_premix_long_context_rope_sampled(T):
@@ -107,10 +119,17 @@ def test_premix_long_context_rope_sampled(T):
         assert_bf16_close(y[:, sl], ref, f"fwd rope@{n0}")
     dy = S.normal((sh.B, sh.N, sh.HP, sh.d), 5, 2)
     dx = to_f64(T.premix_bwd_dx(to_dev(dy), to_dev(w), rope=True, rope_base=S.ROPE_BASE))
+    dx2, dw2 = T.premix_bwd(to_dev(dy), to_dev(x), to_dev(w), rope=True, rope_base=S.ROPE_BASE)
+    dx2 = to_f64(dx2)
     for n0 in (0, sh.N - 67):
         sl = slice(n0, n0 + 67)
         ref = O.premix_bwd_dx(dy[:, sl], w, rope=True, rope_base=S.ROPE_BASE, pos0=n0)
         assert_bf16_close(dx[:, sl], ref, f"dx rope@{n0}")
+        assert_bf16_close(dx2[:, sl], ref, f"fused dx rope@{n0}")
+    # dW with RoPE at this size: the full oracle reduction over 32768 tokens
+    absum = 2.0 * O.premix_bwd_dw(abs_bits(dy), abs_bits(x), sh.P)
+    assert_dw_close(to_f64(dw2), O.premix_bwd_dw(dy, x, sh.P, rope=True, rope_base=S.ROPE_BASE),
+                    absum, "fused dw rope")
 
 
 def test_premix_one_hot_copies_are_bit_exact(T):

@@ -5,7 +5,8 @@ step runs in the library's CUDA kernels; there is no CPU or PyTorch fallback.
 If the library is missing, ``lib()`` raises instead of degrading.
 
 Entry points (same names as the C ABI in include/iha.h):
-  premix_fwd, premix_bwd_dx, premix_bwd_dw   -- "IHA-CUDA", section
+  premix_fwd, premix_bwd_dx, premix_bwd_dw,
+  premix_bwd (both gradients, one pass)     -- "IHA-CUDA", section
       "Pseudo-Token Mixing (Triton Premix Kernels)"
   mha_fwd                                   -- "IHA-CUDA", sections "Kernel
       Design" and "FLOP Matching"; hiera-optim MaskUnitAttentionFast.forward
@@ -20,7 +21,7 @@ import os
 
 from . import _build
 
-__all__ = ["build", "lib", "premix_fwd", "premix_bwd_dx", "premix_bwd_dw", "mha_fwd",
+__all__ = ["build", "lib", "premix_fwd", "premix_bwd_dx", "premix_bwd_dw", "premix_bwd", "mha_fwd",
            "mu_gather", "mu_scatter", "device_error", "IHAError", "Strides", "MASK_NONE",
            "MASK_CAUSAL", "MASK_CAUSAL_WINDOW", "F32", "BF16"]
 
@@ -28,8 +29,9 @@ IHA_OK, IHA_ERR_INVALID_ARG, IHA_ERR_UNSUPPORTED, IHA_ERR_ALIGNMENT, IHA_ERR_CUD
 F32, BF16 = 0, 1
 MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW = 0, 1, 2
 
-SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "mha_fwd", "mu_gather",
-           "mu_scatter", "iha_status_string", "iha_last_error", "iha_device_error")
+SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",
+           "mha_fwd", "mu_gather", "mu_scatter", "iha_status_string", "iha_last_error",
+           "iha_device_error")
 
 
 class IHAError(RuntimeError):
@@ -64,12 +66,13 @@ def lib() -> C.CDLL:
     L.iha_premix_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.iha_premix_bwd_dx.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.iha_premix_bwd_dw.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    L.iha_premix_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.mha_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, Strides, Strides, Strides,
                           Strides, f, i, i, i, vp]
     L.mu_gather.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     L.mu_scatter.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
-    for name in ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "mha_fwd",
-                 "mu_gather", "mu_scatter"):
+    for name in ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",
+                 "mha_fwd", "mu_gather", "mu_scatter"):
         getattr(L, name).restype = C.c_int
     L.iha_status_string.argtypes = [i]
     L.iha_status_string.restype = C.c_char_p
@@ -166,6 +169,23 @@ def premix_bwd_dw(dy, x, P: int, rope: bool = False, rope_base: float = 10000.0,
                                   int(rope), float(rope_base), _stream(stream)),
           "iha_premix_bwd_dw")
     return out
+
+
+def premix_bwd(dy, x, w, rope: bool = False, rope_base: float = 10000.0, dx=None, dw=None,
+               stream=None):
+    """(dX, dW) in one pass over dY: dX = W^T dY (inverse RoPE when rope), dW = sum dY X^T."""
+    torch = _torch()
+    _need_cuda(dy, x, w)
+    B, N, H, d = x.shape
+    P = w.shape[1]
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        dw = torch.empty((H, P, H), dtype=torch.float32, device=x.device)
+    check(lib().iha_premix_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(dx), _ptr(dw), B, N, H, P, d,
+                               _dt(x), int(rope), float(rope_base), _stream(stream)),
+          "iha_premix_bwd")
+    return dx, dw
 
 
 # ---------------------------------------------------------------- attention

@@ -241,23 +241,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + (uint32_t)(t * 128);
     const uint32_t tO = tmem + lane_base + (uint32_t)(256 + t * 128);
     const int tq_lo = qt * kBM, tq_hi = min(tq_lo + kBM - 1, p.Nq - 1);
-    float m_used = -INFINITY, l = 0.f;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY;  // running row maximum, log2 units (scale included)
+    float l = 0.f;             // running row sum relative to m_used
     bool ok = (t == 0) || act1;
     for (int it = 0; ok && it < n_kv; ++it) {
       const int k0 = (j_lo + it) * kBN;
       if (!(ok = mbar_wait(b_sfull(t), it & 1, abort_flag))) break;
       tc_fence_after();
-      float x[128];
-      {
-        uint32_t r[32];
+      uint32_t s[128];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tS + 32u * c, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(r[e]) * p.scale_log2;
-        }
-      }
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s + 32 * c);
+      tmem_wait_ld();
       const bool full_tile =
           (k0 + kBN <= p.Nk) &&
           (p.mask == IHA_MASK_NONE ||
@@ -272,50 +267,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             vis = vis && kj <= i;
             if (p.mask == IHA_MASK_CAUSAL_WINDOW) vis = vis && (i - kj < p.window);
           }
-          if (!vis) x[e] = -INFINITY;
+          if (!vis) s[e] = 0xFF800000u;  // -inf
         }
       }
-      float mt = x[0];
+      float mt = __uint_as_float(s[0]);
 #pragma unroll
-      for (int e = 1; e < 128; ++e) mt = fmaxf(mt, x[e]);
-      const float m_new = fmaxf(m_used, mt);
+      for (int e = 1; e < 128; ++e) mt = fmaxf(mt, __uint_as_float(s[e]));
+      const float m_new = fmaxf(m_used, mt * sl2);
+      bool rescale = false;
+      float factor = 1.f;
       if (it == 0) {
         m_used = m_new;
-      } else {
-        const bool need = m_new > m_used + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          const float factor = (m_new == -INFINITY) ? 1.f : fast_exp2(m_used - m_new);
-          l *= factor;
-          m_used = m_new;
-          uint32_t r[32];
-          for (int c = 0; c < 2 * p.nD; ++c) {
-            tmem_ld32(tO + 32u * c, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
-            tmem_st32(tO + 32u * c, r);
-          }
-          tmem_wait_st();
-        }
+      } else if (__any_sync(0xffffffffu, m_new > m_used + kRescaleLog2)) {
+        factor = (m_new == -INFINITY) ? 1.f : fast_exp2(m_used - m_new);
+        l *= factor;
+        m_used = m_new;
+        rescale = true;
       }
       const float base = (m_used == -INFINITY) ? 0.f : m_used;
-      float sum = 0.f;
-      {
-        uint32_t pk[32];
+      // P = 2^(s * scale_log2 - base), packed to bf16 pairs over the S columns
+      const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(-base, -base);
+      float2 sum2 = make_float2(0.f, 0.f);
+      uint32_t pk[64];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+      for (int e = 0; e < 64; ++e) {
+        const float2 xx = __ffma2_rn(
+            make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nb2);
+        const float p0 = fast_exp2(xx.x), p1 = fast_exp2(xx.y);
+        sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
+        pk[e] = pack_bf16x2(p0, p1);
+      }
+      tmem_st32(tS, pk);
+      tmem_st32(tS + 32u, pk + 32);
+      l += sum2.x + sum2.y;
+      if (rescale) {
+        // O <- O * factor before this tile's P.V is issued (PV of the previous
+        // tile is complete: the S commit waited on above tracks it)
+        uint32_t r[32];
+        for (int c = 0; c < 2 * p.nD; ++c) {
+          tmem_ld32(tO + 32u * c, r);
+          tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float p0 = fast_exp2(x[64 * c + 2 * e] - base);
-            const float p1 = fast_exp2(x[64 * c + 2 * e + 1] - base);
-            sum += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
-          }
-          tmem_st32(tS + 32u * c, pk);
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
+          tmem_st32(tO + 32u * c, r);
         }
       }
       tmem_wait_st();
-      l += sum;
       tc_fence_before();
       mbar_arrive(b_pfull(t));
     }
@@ -325,22 +322,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.o + bo * p.so_bo + bi * p.so_bi + (int64_t)i * p.so_seq + h * p.so_h;
-      uint32_t r[32];
-      for (int c = 0; c < 2 * p.nD; ++c) {
-        tmem_ld32(tO + 32u * c, r);
-        tmem_wait_ld();
-        if (ok && i < p.Nq) {
+      uint32_t r[128];
+      tmem_ld32(tO, r);
+      tmem_ld32(tO + 32u, r + 32);
+      if (p.nD == 2) {
+        tmem_ld32(tO + 64u, r + 64);
+        tmem_ld32(tO + 96u, r + 96);
+      }
+      tmem_wait_ld();
+      if (ok && i < p.Nq) {
 #pragma unroll
-          for (int g8 = 0; g8 < 4; ++g8) {
-            const int f = 32 * c + 8 * g8;
-            if (f < p.d) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[8 * g8 + 0]) * inv_l, __uint_as_float(r[8 * g8 + 1]) * inv_l);
-              v.y = pack_bf16x2(__uint_as_float(r[8 * g8 + 2]) * inv_l, __uint_as_float(r[8 * g8 + 3]) * inv_l);
-              v.z = pack_bf16x2(__uint_as_float(r[8 * g8 + 4]) * inv_l, __uint_as_float(r[8 * g8 + 5]) * inv_l);
-              v.w = pack_bf16x2(__uint_as_float(r[8 * g8 + 6]) * inv_l, __uint_as_float(r[8 * g8 + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(orow + f) = v;
-            }
+        for (int g8 = 0; g8 < 16; ++g8) {
+          const int f = 8 * g8;
+          if (f < p.d) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[f + 0]) * inv_l, __uint_as_float(r[f + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(r[f + 2]) * inv_l, __uint_as_float(r[f + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(r[f + 4]) * inv_l, __uint_as_float(r[f + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(r[f + 6]) * inv_l, __uint_as_float(r[f + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + f) = v;
           }
         }
       }

@@ -16,6 +16,7 @@
 // the inverse rotation after the transposed mix and the weight gradient
 // rotates X instead of dY (<R^T a, b> = <a, R b>).
 #include "common.cuh"
+#include "premix_tc.h"
 
 namespace iha {
 namespace {
@@ -583,6 +584,8 @@ iha_status iha_premix_fwd(const void* x, const float* w, void* y, int B, int N, 
       overlaps(y, g.ntok * g.HP * d * es, w, (size_t)g.HP * H * 4))
     return fail(IHA_ERR_INVALID_ARG, "iha_premix_fwd: y overlaps an input");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == IHA_BF16 && premix_tc_supported(H, P, d))
+    return premix_fwd_tc(x, w, y, B, N, H, P, d, rope, rope_base, s);
   if (dt == IHA_BF16) launch_fwd<__nv_bfloat16>(g, x, w, y, rope != 0, s);
   else launch_fwd<float>(g, x, w, y, rope != 0, s);
   return check_launch("iha_premix_fwd");
@@ -600,6 +603,8 @@ iha_status iha_premix_bwd_dx(const void* dy, const float* w, void* dx, int B, in
       overlaps(dx, g.ntok * H * d * es, w, (size_t)g.HP * H * 4))
     return fail(IHA_ERR_INVALID_ARG, "iha_premix_bwd_dx: dx overlaps an input");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == IHA_BF16 && premix_bwd_tc_supported(H, P, d))
+    return premix_bwd_tc(dy, nullptr, w, dx, nullptr, B, N, H, P, d, rope, rope_base, s);
   if (dt == IHA_BF16) launch_dx<__nv_bfloat16>(g, dy, w, dx, rope != 0, s);
   else launch_dx<float>(g, dy, w, dx, rope != 0, s);
   return check_launch("iha_premix_bwd_dx");
@@ -619,6 +624,8 @@ iha_status iha_premix_bwd_dw(const void* dy, const void* x, float* dw, int B, in
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dt == IHA_BF16) {
     zero_f32_kernel<<<1, 256, 0, s>>>(dw, g.HP * H);
+    if (premix_bwd_tc_supported(H, P, d))
+      return premix_bwd_tc(dy, x, nullptr, nullptr, dw, B, N, H, P, d, rope, rope_base, s);
     st = launch_dw_mma(g, dy, x, dw, rope != 0, s);
     if (st != IHA_OK) return st;
   } else {
@@ -630,6 +637,31 @@ iha_status iha_premix_bwd_dw(const void* dy, const void* x, float* dw, int B, in
                                                            static_cast<const float*>(x), dw, g);
   }
   return check_launch("iha_premix_bwd_dw");
+}
+
+iha_status iha_premix_bwd(const void* dy, const void* x, const float* w, void* dx, float* dw,
+                          int B, int N, int H, int P, int d, iha_dtype dt, int rope,
+                          float rope_base, void* stream) {
+  using namespace iha;
+  iha_status st = check_common("iha_premix_bwd", dy, x, dx, B, N, H, P, d, dt, rope, rope_base);
+  if (st != IHA_OK) return st;
+  if (!w || !dw) return fail(IHA_ERR_INVALID_ARG, "iha_premix_bwd: null pointer");
+  if (!aligned16(dw)) return fail(IHA_ERR_ALIGNMENT, "iha_premix_bwd: dw must be 16-byte aligned");
+  const PremixGeom g = make_geom(B, N, H, P, d, rope_base);
+  const size_t es = dt == IHA_BF16 ? 2 : 4;
+  const size_t nx = g.ntok * H * d * es, ny = g.ntok * g.HP * d * es, nw = (size_t)g.HP * H * 4;
+  if (overlaps(dx, nx, dy, ny) || overlaps(dx, nx, x, nx) || overlaps(dx, nx, w, nw) ||
+      overlaps(dw, nw, dy, ny) || overlaps(dw, nw, x, nx) || overlaps(dw, nw, w, nw) ||
+      overlaps(dw, nw, dx, nx))
+    return fail(IHA_ERR_INVALID_ARG, "iha_premix_bwd: an output overlaps another buffer");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == IHA_BF16 && premix_bwd_tc_supported(H, P, d)) {
+    zero_f32_kernel<<<1, 256, 0, s>>>(dw, g.HP * H);
+    return premix_bwd_tc(dy, x, w, dx, dw, B, N, H, P, d, rope, rope_base, s);
+  }
+  st = iha_premix_bwd_dx(dy, w, dx, B, N, H, P, d, dt, rope, rope_base, stream);
+  if (st != IHA_OK) return st;
+  return iha_premix_bwd_dw(dy, x, dw, B, N, H, P, d, dt, rope, rope_base, stream);
 }
 
 }  // extern "C"

@@ -1,0 +1,35 @@
+// Internal interface between the premix entry points and the tensor-core
+// premix kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "iha.h"
+
+namespace iha {
+
+// RoPE inverse frequencies inv_freq_i = base^(-2i/d) (i < d/2, up to 64),
+// computed in double on the host and carried as an fp32 pair hi + lo.
+struct RopeTable {
+  float hi[64];
+  float lo[64];
+};
+void make_rope_table(RopeTable* rt, int d, float base);
+
+// Shapes the tensor-core premix handles: bf16, d in {64, 128}, H <= 32,
+// H*P <= 128.
+bool premix_tc_supported(int H, int P, int d);
+
+// Backward shapes: bf16, d = 128, H <= 32, H*P <= 128.
+bool premix_bwd_tc_supported(int H, int P, int d);
+
+// dX (if dx != nullptr) and dW (if dw != nullptr, accumulated with atomics
+// into a zeroed dw) in one pass over dY.
+iha_status premix_bwd_tc(const void* dy, const void* x, const float* w, void* dx, float* dw,
+                         int B, int N, int H, int P, int d, int rope, float rope_base,
+                         cudaStream_t stream);
+
+iha_status premix_fwd_tc(const void* x, const float* w, void* y, int B, int N, int H, int P,
+                         int d, int rope, float rope_base, cudaStream_t stream);
+
+}  // namespace iha
