@@ -270,9 +270,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!vis) s[e] = 0xFF800000u;  // -inf
         }
       }
-      float mt = __uint_as_float(s[0]);
+      // row maximum: 8 independent three-input max chains, then a small tree
+      float mx[8];
 #pragma unroll
-      for (int e = 1; e < 128; ++e) mt = fmaxf(mt, __uint_as_float(s[e]));
+      for (int j = 0; j < 8; ++j) mx[j] = __uint_as_float(s[j]);
+#pragma unroll
+      for (int e = 8; e < 128; e += 16)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          mx[j] = fmax3f(mx[j], __uint_as_float(s[e + j]), __uint_as_float(s[e + 8 + j]));
+      const float mt = fmaxf(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], fmax3f(mx[5], mx[6], mx[7])));
       const float m_new = fmaxf(m_used, mt * sl2);
       bool rescale = false;
       float factor = 1.f;
@@ -287,19 +294,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float base = (m_used == -INFINITY) ? 0.f : m_used;
       // P = 2^(s * scale_log2 - base), packed to bf16 pairs over the S columns
       const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(-base, -base);
-      float2 sum2 = make_float2(0.f, 0.f);
+      float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
       uint32_t pk[64];
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
         const float2 xx = __ffma2_rn(
             make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nb2);
         const float p0 = fast_exp2(xx.x), p1 = fast_exp2(xx.y);
-        sum2 = __fadd2_rn(sum2, make_float2(p0, p1));
+        sum2[e & 3] = __fadd2_rn(sum2[e & 3], make_float2(p0, p1));
         pk[e] = pack_bf16x2(p0, p1);
       }
       tmem_st32(tS, pk);
       tmem_st32(tS + 32u, pk + 32);
-      l += sum2.x + sum2.y;
+      const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+      const float2 st = __fadd2_rn(s01, s23);
+      l += st.x + st.y;
       if (rescale) {
         // O <- O * factor before this tile's P.V is issued (PV of the previous
         // tile is complete: the S commit waited on above tracks it)
