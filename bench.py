@@ -3,30 +3,36 @@
 
 One step = one pass of every hot-path operation over one batch of seeded
 synthetic inputs, each at its workload's shape:
-  premix   LLaMA-2.4B layer shape B=1, N=8192, H=20, P=4, d=128:
-           forward for Q and K (fused RoPE, base 10000) and V; backward (input
-           gradient with inverse RoPE for Q, K, and weight gradient) for Q, K, V,
-           both gradients from one pass over dY;
-  attention 80 pseudo-heads, N=4096, d=128, causal window W=1024, fp32 LSE;
-  Hiera    MAE stage 1, B=128, 56x56 tokens, 8x8 units, 20 kept, C=d=96:
-           gather, attention inside each unit, scatter.
-The step's working set (~1.7 GB) is far larger than L2 (129 MB), so no L2
+  premix     LLaMA-2.4B layer shape B=1, N=8192, H=20, P=4, d=128: forward
+             for Q and K (fused RoPE, base 10000) and V; backward (input
+             gradient, inverse RoPE for Q and K, and weight gradient from the
+             same pass over dY) for Q, K, V;
+  attention  80 pseudo-heads, N=4096, d=128, causal window W=1024, fp32 LSE;
+  Hiera      MAE stage 1, B=128, 56x56 tokens, 8x8 units, 20 kept, C=d=96:
+             gather, attention inside each unit, scatter;
+  long ctx   the long-context IHA layer forward, B=2, N=16384, H=20, P=4,
+             d=128: premix Q and K with RoPE and V, then causal attention over
+             the 80 pseudo-heads on those premix outputs (fp32 LSE).
+The step's working set (~5 GB) is far larger than L2 (129 MB), so no L2
 flush is needed between steps: every op's inputs were evicted by the others.
+The tiny fp32 layer (B=1, N=128, H=4, P=2, d=32: premix Q, K, V and unmasked
+attention) is latency-bound; its time per layer is reported separately.
 
 Metric: every op has an algorithmic roofline time, max(bytes / HBM peak,
-flops / bf16 peak) with the measured peaks; the step's efficiency is the sum
-of those times over the measured step time.  `value` is that efficiency in %
-summed over GPUs (so it adds up across replicas; at N=1 it is the
-efficiency).  Per-op GB/s and TFLOP/s are in `ops`.
+flops / bf16 peak) with the measured peaks (burst: the timed region lasts
+well under a second); the step's efficiency is the sum of those times over
+the measured step time.  `value` is that efficiency in % summed over GPUs (it
+adds up across replicas; at N=1 it is the efficiency).  Per-op GB/s, TFLOP/s
+and roofline fractions are in `ops`.
 
---impl reference times the oracle (CPU) on a bounded sample of the same step
-and extrapolates; it is a deliberately slow baseline, not a target.
+--impl reference times the oracle (CPU) on a bounded random sample of the
+same step and scales it to the whole step; it is a deliberately slow
+baseline, not a target.
 """
 from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -43,9 +49,13 @@ import synthetic as S  # noqa: E402
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
 METRIC = "premix+gather GB/s and attention TFLOP/s at 1 GB300, as % of roofline"
+UNIT = "% of 1-GPU roofline, summed over GPUs"
+# Fraction of every op the oracle runs per CPU sample (same in both CPU legs).
+CPU_FRAC = 1 / 256
 
-# dram bytes (read + write) per launch from ncu captures of the current kernels
-# (see profiles/); None where no capture of the current kernel exists.
+# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
+# capture summarised in profiles/ (None until a capture of the current kernel
+# exists; reset whenever that kernel changes).
 NCU_TRAFFIC = {}
 
 
@@ -53,52 +63,67 @@ def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
-            d = json.load(f)
-        return d, "measured"
+            return json.load(f), "measured"
     return dict(FALLBACK_PEAKS), "fallback"
 
 
 # --------------------------------------------------------------------------- workload
+def _attn_pairs(N: int, mask: str, W: int = 0) -> int:
+    """Visible (query, key) pairs of one head."""
+    if mask == "causal":
+        return N * (N + 1) // 2
+    return sum(min(i + 1, W) for i in range(N))
+
+
 def op_table():
-    """(name, kind, algorithmic bytes, algorithmic flops) per op of one step."""
+    """(name, bytes, flops) per op of one step, algorithmic (inputs read once,
+    outputs written once)."""
+    ops = []
     pm = S.LLAMA_PREMIX
     tok = pm.B * pm.N
-    x_b = tok * pm.H * pm.d * 2
-    y_b = tok * pm.HP * pm.d * 2
-    w_b = pm.HP * pm.H * 4
-    premix_flops = 2 * tok * pm.HP * pm.H * pm.d
-    ops = []
-    for t in ("q", "k", "v"):
-        ops.append((f"premix_fwd_{t}", "premix", x_b + y_b + w_b, premix_flops))
-    for t in ("q", "k", "v"):   # dX and dW from one read of dY and X
-        ops.append((f"premix_bwd_{t}", "premix", y_b + 2 * x_b + 2 * w_b, 2 * premix_flops))
+    x_b, y_b, w_b = tok * pm.H * pm.d * 2, tok * pm.HP * pm.d * 2, pm.HP * pm.H * 4
+    pf = 2 * tok * pm.HP * pm.H * pm.d
+    for t in "qkv":
+        ops.append((f"premix_fwd_{t}", x_b + y_b + w_b, pf))
+    for t in "qkv":   # dX and dW from one read of dY and X
+        ops.append((f"premix_bwd_{t}", y_b + 2 * x_b + 2 * w_b, 2 * pf))
     aw = S.LLAMA_WINDOW
-    W = S.WINDOW_KEYS
-    pairs = sum(min(i + 1, W) for i in range(aw.N))
-    attn_flops = 4 * aw.d * pairs * aw.HP
-    attn_bytes = 4 * aw.B * aw.N * aw.HP * aw.d * 2 + aw.B * aw.HP * aw.N * 4
-    ops.append(("attention_window", "attention", attn_bytes, attn_flops))
+    ops.append(("attention_window",
+                4 * aw.B * aw.N * aw.HP * aw.d * 2 + aw.B * aw.HP * aw.N * 4,
+                4 * aw.d * _attn_pairs(aw.N, "window", S.WINDOW_KEYS) * aw.HP * aw.B))
     mu = S.HIERA_MU
     kept = mu.B * mu.n_keep * mu.unit_tokens * mu.C * 2
-    ops.append(("mu_gather", "gather", 2 * kept + mu.B * mu.n_keep * 4, 0))
-    mu_flops = 4 * mu.C * mu.unit_tokens * mu.unit_tokens * mu.B * mu.n_keep
-    ops.append(("mu_attention", "attention", 4 * kept, mu_flops))
-    ops.append(("mu_scatter", "gather", 2 * kept + mu.B * mu.n_keep * 4, 0))
+    ops.append(("mu_gather", 2 * kept + mu.B * mu.n_keep * 4, 0))
+    ops.append(("mu_attention", 4 * kept,
+                4 * mu.C * mu.unit_tokens * mu.unit_tokens * mu.B * mu.n_keep))
+    ops.append(("mu_scatter", 2 * kept + mu.B * mu.n_keep * 4, 0))
+    lc = S.LONG_CTX
+    tok = lc.B * lc.N
+    x_b, y_b = tok * lc.H * lc.d * 2, tok * lc.HP * lc.d * 2
+    pf = 2 * tok * lc.HP * lc.H * lc.d
+    for t in "qkv":
+        ops.append((f"long_premix_fwd_{t}", x_b + y_b + w_b, pf))
+    ops.append(("long_attention_causal", 4 * y_b + lc.B * lc.HP * lc.N * 4,
+                4 * lc.d * _attn_pairs(lc.N, "causal") * lc.HP * lc.B))
     return ops
 
 
-LAUNCHES_PER_STEP = 3 + 3 * 2 + 1 + 3   # premix fwd, bwd (zero dW + kernel), attention, MU x3
+def launches_per_step() -> int:
+    # premix fwd 3; premix bwd 3 x (zero dW + kernel); window attention;
+    # gather, MU attention, scatter; long-context premix 3 + attention
+    return 3 + 3 * 2 + 1 + 3 + 3 + 1
 
 
 def host_inputs(seed: int):
-    pm, aw, mu = S.LLAMA_PREMIX, S.LLAMA_WINDOW, S.HIERA_MU
+    pm, aw, mu, lc = S.LLAMA_PREMIX, S.LLAMA_WINDOW, S.HIERA_MU, S.LONG_CTX
     d = {}
     for c, t in enumerate("qkv"):
         d[f"x_{t}"] = S.normal((pm.B, pm.N, pm.H, pm.d), seed, 10 + c)
         d[f"w_{t}"] = S.premix_weight(pm.H, pm.P, seed, 20 + c)
         d[f"dy_{t}"] = S.normal((pm.B, pm.N, pm.HP, pm.d), seed, 30 + c)
-    for c, t in enumerate("qkv"):
         d[f"a_{t}"] = S.normal((aw.B, aw.N, aw.HP, aw.d), seed, 40 + c)
+        d[f"lx_{t}"] = S.normal((lc.B, lc.N, lc.H, lc.d), seed, 60 + c)
+        d[f"lw_{t}"] = S.premix_weight(lc.H, lc.P, seed, 70 + c)
     d["mu_x"] = S.normal((mu.B, mu.grid_h * mu.grid_w, mu.C), seed, 50)
     d["mu_keep"] = S.keep_units(mu.B, mu.n_units, mu.n_keep, seed)
     return d
@@ -123,10 +148,11 @@ def gpu_id(torch, device) -> str:
 
 
 class Step:
-    """Device buffers and the launch sequence of one step."""
+    """Device buffers and the launch sequence of one step (every op through the
+    package's public calls)."""
 
     def __init__(self, T, torch, dev_inputs, device):
-        pm, aw, mu = S.LLAMA_PREMIX, S.LLAMA_WINDOW, S.HIERA_MU
+        pm, aw, mu, lc = S.LLAMA_PREMIX, S.LLAMA_WINDOW, S.HIERA_MU, S.LONG_CTX
         self.T, self.torch = T, torch
         self.i = dev_inputs
         e = lambda shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device=device)
@@ -139,42 +165,54 @@ class Step:
         self.ou = e((mu.B, mu.n_keep, mu.unit_tokens, mu.C))
         self.dec = torch.zeros((mu.B, mu.grid_h * mu.grid_w, mu.C), dtype=torch.bfloat16,
                                device=device)
+        self.ly = {t: e((lc.B, lc.N, lc.HP, lc.d)) for t in "qkv"}
+        self.lo = e((lc.B, lc.N, lc.HP, lc.d))
+        self.llse = e((lc.B, 1, lc.HP, lc.N), torch.float32)
 
-    def outputs(self):
+    def results(self):
+        """What a caller reads back: every op's final output (the long-context
+        premix outputs are intermediates consumed by its attention)."""
         return ([self.y[t] for t in "qkv"] + [self.dx[t] for t in "qkv"] +
-                [self.dw[t] for t in "qkv"] + [self.o, self.lse, self.dec])
+                [self.dw[t] for t in "qkv"] + [self.o, self.lse, self.dec, self.lo, self.llse])
 
     def run(self, marks=None):
-        """Enqueue the step; `marks(i)` records an event after op i (and before op 0)."""
+        """Enqueue the step; `marks(k)` records an event before op 0 and after op k-1."""
         T, i = self.T, self.i
-        pm, aw, mu = S.LLAMA_PREMIX, S.LLAMA_WINDOW, S.HIERA_MU
+        pm, aw, mu, lc = S.LLAMA_PREMIX, S.LLAMA_WINDOW, S.HIERA_MU, S.LONG_CTX
         mark = marks or (lambda k: None)
         k = 0
         mark(k)
+
+        def done():
+            nonlocal k
+            k += 1
+            mark(k)
+
         for t in "qkv":
             T.premix_fwd(i[f"x_{t}"], i[f"w_{t}"], pm.P, rope=(t != "v"), rope_base=S.ROPE_BASE,
                          out=self.y[t])
-            k += 1
-            mark(k)
+            done()
         for t in "qkv":
             T.premix_bwd(i[f"dy_{t}"], i[f"x_{t}"], i[f"w_{t}"], rope=(t != "v"),
                          rope_base=S.ROPE_BASE, dx=self.dx[t], dw=self.dw[t])
-            k += 1
-            mark(k)
+            done()
         T.mha_fwd(i["a_q"], i["a_k"], i["a_v"], mask=T.MASK_CAUSAL_WINDOW, window=S.WINDOW_KEYS,
                   out=self.o, lse=self.lse)
-        k += 1
-        mark(k)
+        done()
         T.mu_gather(i["mu_x"], i["mu_keep"], mu.grid_h, mu.grid_w, mu.mu_h, mu.mu_w, out=self.g)
-        k += 1
-        mark(k)
+        done()
         u = self.g.view(mu.B * mu.n_keep, 1, mu.unit_tokens, 1, mu.C)
         T.mha_fwd(u, u, u, out=self.ou.view(mu.B * mu.n_keep, 1, mu.unit_tokens, 1, mu.C))
-        k += 1
-        mark(k)
+        done()
         T.mu_scatter(self.ou, i["mu_keep"], self.dec, mu.grid_h, mu.grid_w, mu.mu_h, mu.mu_w)
-        k += 1
-        mark(k)
+        done()
+        for t in "qkv":
+            T.premix_fwd(i[f"lx_{t}"], i[f"lw_{t}"], lc.P, rope=(t != "v"),
+                         rope_base=S.ROPE_BASE, out=self.ly[t])
+            done()
+        T.mha_fwd(self.ly["q"], self.ly["k"], self.ly["v"], mask=T.MASK_CAUSAL, out=self.lo,
+                  lse=self.llse)
+        done()
 
 
 class ClockSampler:
@@ -186,7 +224,6 @@ class ClockSampler:
     def __init__(self, index: str):
         self.index = index
         self.proc = None
-        self.lines = []
 
     def start(self):
         try:
@@ -226,6 +263,36 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def tiny_layer_latency(T, torch, device, iters: int = 50):
+    """Tiny fp32 IHA layer forward (premix Q, K, V into 8 pseudo-heads, then
+    unmasked attention): microseconds per layer (4 launches), CUDA events."""
+    sh = S.TINY
+    xs = [host_tensor(S.normal((sh.B, sh.N, sh.H, sh.d), 0, c, dtype="f32"), torch).to(device)
+          for c in range(3)]
+    ws = [host_tensor(S.premix_weight(sh.H, sh.P, 0, 10 + c), torch).to(device) for c in range(3)]
+    ys = [torch.empty((sh.B, sh.N, sh.HP, sh.d), dtype=torch.float32, device=device)
+          for _ in range(3)]
+    o = torch.empty_like(ys[0])
+
+    def layer():
+        for x, w, y in zip(xs, ws, ys):
+            T.premix_fwd(x, w, sh.P, out=y)
+        T.mha_fwd(*ys, out=o)
+
+    for _ in range(5):
+        layer()
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        layer()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    return {"us_per_layer": round(e0.elapsed_time(e1) * 1e3 / iters, 2), "launches": 4,
+            "config": "B=1, N=128, H=4, P=2, d=32, fp32, unmasked"}
+
+
 def gpu_arm(args, rank, world, local_rank):
     import torch
     import transformer_attention_iha_gb300 as T
@@ -235,10 +302,11 @@ def gpu_arm(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     peaks, peak_src = load_peaks()
     hbm = peaks["hbm_gbs"] * 1e9
-    tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 1e12
+    tc = peaks["bf16_tflops"] * 1e12   # burst: the timed region is well under a second
 
     host = host_inputs(seed=rank)
     hostt = {k: host_tensor(v, torch) for k, v in host.items()}
+    del host
     dev = {k: v.to(device) for k, v in hostt.items()}
     step = Step(T, torch, dev, device)
     stream = torch.cuda.current_stream(device)
@@ -251,8 +319,8 @@ def gpu_arm(args, rank, world, local_rank):
     if T.device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
-    # per-op events: K x (nops + 1)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)]
+           for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(gpu_id(torch, device))
     clocks.start()
@@ -278,26 +346,23 @@ def gpu_arm(args, rank, world, local_rank):
              for k in range(nops)]
     derr = T.device_error()
 
-    # roofline per op and for the step
-    op_out = {}
-    ideal_total = 0.0
-    for (name, kind, nbytes, flops), ms in zip(ops, op_ms):
-        t_hbm = nbytes / hbm
-        t_tc = flops / tc if flops else 0.0
+    op_out, ideal_total = {}, 0.0
+    for (name, nbytes, flops), ms in zip(ops, op_ms):
+        t_hbm, t_tc = nbytes / hbm, (flops / tc if flops else 0.0)
         ideal = max(t_hbm, t_tc)
         ideal_total += ideal
         rec = {"ms": round(ms, 5), "roofline_ms": round(ideal * 1e3, 5),
-               "frac": round(ideal / (ms * 1e-3), 4)}
-        rec["GB/s"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+               "frac": round(ideal / (ms * 1e-3), 4),
+               "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+               "bound": "tensor" if t_tc > t_hbm else "hbm"}
         if flops:
             rec["TFLOP/s"] = round(flops / (ms * 1e-3) / 1e12, 1)
-        rec["bound"] = "tensor" if t_tc > t_hbm else "hbm"
         op_out[name] = rec
     eff = ideal_total / (ms_step * 1e-3)
 
     # dominant kernel by time share
     dom = max(range(nops), key=lambda k: op_ms[k])
-    dname, dkind, dbytes, dflops = ops[dom]
+    dname, dbytes, dflops = ops[dom]
     dsec = op_ms[dom] * 1e-3
     if op_out[dname]["bound"] == "tensor":
         roof = {"bound": "tensor", "achieved": round(dflops / dsec / 1e12, 1),
@@ -308,21 +373,24 @@ def gpu_arm(args, rank, world, local_rank):
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = NCU_TRAFFIC.get(dname)
     roof["kernel"] = dname
-    roof["peak_source"] = peak_src + (" sustained" if roof["bound"] == "tensor" else "")
+    roof["share"] = round(op_ms[dom] / ms_step, 4)
+    roof["peak_source"] = f"{peak_src} ({'bf16 burst' if roof['bound'] == 'tensor' else 'copy'})"
 
-    # end to end: host buffers, H2D of every input and D2H of every output per step
+    tiny = tiny_layer_latency(T, torch, device)
+
+    # end to end: host buffers; every input copied in and every result read back per step
     e2e = None
     if args.e2e_steps > 0:
         pinned = {k: v.pin_memory() for k, v in hostt.items()}
-        outs_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in step.outputs()]
+        res_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in step.results()]
         h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-        d2h = sum(o.numel() * o.element_size() for o in outs_host)
+        d2h = sum(o.numel() * o.element_size() for o in res_host)
 
         def e2e_step():
             for k, v in pinned.items():
                 dev[k].copy_(v, non_blocking=True)
             step.run()
-            for o, h in zip(step.outputs(), outs_host):
+            for o, h in zip(step.results(), res_host):
                 h.copy_(o, non_blocking=True)
 
         e2e_step()
@@ -340,14 +408,14 @@ def gpu_arm(args, rank, world, local_rank):
             t = torch.tensor([e2e_ms], device=device)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             e2e_ms = float(t.item())
-        e2e = {"value": round(100.0 * ideal_total / (e2e_ms * 1e-3) * world, 3),
-               "unit": "% of 1-GPU roofline, summed over GPUs", "ms_per_step": round(e2e_ms, 4),
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        e2e = {"value": round(100.0 * ideal_total / (e2e_ms * 1e-3) * world, 3), "unit": UNIT,
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
 
     line = {
         "metric": METRIC,
         "value": round(100.0 * eff * world, 3),
-        "unit": "% of 1-GPU roofline, summed over GPUs",
+        "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -355,66 +423,96 @@ def gpu_arm(args, rank, world, local_rank):
         "config": {"workload": "IHA hot-path step: premix fwd(+RoPE) and fused dX+dW for Q,K,V at "
                                "B=1,N=8192,H=20,P=4,d=128; causal-window attention 80 heads "
                                "N=4096 d=128 W=1024; Hiera-Base MAE stage-1 gather + mask-unit "
-                               "attention (2560 units x 64 tokens, d=96) + scatter",
-                   "l2": "no flush: step working set ~1.7 GB > 129 MB L2",
+                               "attention (2560 units x 64 tokens, d=96) + scatter; long-context "
+                               "layer B=2,N=16384: premix Q,K(+RoPE),V and causal attention over "
+                               "80 pseudo-heads",
+                   "l2": "no flush: step working set ~5 GB > 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "ops": op_out,
         "roofline": roof,
+        "tiny_layer_fp32": tiny,
         "e2e": e2e,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": launches_per_step() * args.steps,
         "clocks": clk,
         "device_error": derr,
-        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops_sustained": tc / 1e12,
+        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
                   "source": peak_src},
     }
-    return line, step
+    return line
 
 
 # --------------------------------------------------------------------------- CPU (oracle) arm
-def oracle_sample(host, frac: float):
-    """Time the oracle on a bounded sample of one step and extrapolate.
-
-    Returns (extrapolated seconds per full step, sample description, threads)."""
+def oracle_sample(host, frac: float, seed: int = 0):
+    """Time the oracle on a random `frac` of every op of one step and scale each
+    op's time by its sampled share.  Returns (seconds per full step, measured
+    seconds, sample description, threads)."""
     import oracle as O
-    pm, aw, mu = S.LLAMA_PREMIX, S.LLAMA_WINDOW, S.HIERA_MU
+    pm, aw, mu, lc = S.LLAMA_PREMIX, S.LLAMA_WINDOW, S.HIERA_MU, S.LONG_CTX
+    g = np.random.default_rng(seed)
+    t_full = t_meas = 0.0
+
+    def timed(fn, scale):
+        nonlocal t_full, t_meas
+        t0 = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t0
+        t_meas += dt
+        t_full += dt * scale
+
+    def attn_rows(q, k, v, heads, N, B, mask, window, nrows):
+        rows = np.stack([g.integers(0, B, nrows), np.zeros(nrows, np.int64),
+                         g.integers(0, heads, nrows), g.integers(0, N, nrows)], axis=1)
+        O.attention_rows(q[:, None], k[:, None], v[:, None], rows.astype(np.int64), mask, window)
+
     ntok = max(1, int(pm.N * frac))
-    t_total = 0.0
     for t in "qkv":
         rope = t != "v"
         x, w, dy = host[f"x_{t}"][:, :ntok], host[f"w_{t}"], host[f"dy_{t}"][:, :ntok]
-        t0 = time.perf_counter()
-        O.premix_fwd(x, w, pm.P, rope=rope, rope_base=S.ROPE_BASE)
-        O.premix_bwd_dx(dy, w, rope=rope, rope_base=S.ROPE_BASE)
-        O.premix_bwd_dw(dy, x, pm.P, rope=rope, rope_base=S.ROPE_BASE)
-        t_total += (time.perf_counter() - t0) * (pm.N / ntok)
-    nrows_all = aw.N * aw.HP
-    nrows = max(1, int(nrows_all * frac))
-    g = np.random.default_rng(0)
-    rows = np.stack([np.zeros(nrows, np.int64), np.zeros(nrows, np.int64),
-                     g.integers(0, aw.HP, nrows), g.integers(0, aw.N, nrows)], axis=1)
-    qa, ka, va = (host[f"a_{t}"][:, None] for t in "qkv")
-    t0 = time.perf_counter()
-    O.attention_rows(qa, ka, va, rows, O.MASK_CAUSAL_WINDOW, S.WINDOW_KEYS)
-    t_total += (time.perf_counter() - t0) * (nrows_all / nrows)
+        timed(lambda: O.premix_fwd(x, w, pm.P, rope=rope, rope_base=S.ROPE_BASE), pm.N / ntok)
+        timed(lambda: (O.premix_bwd_dx(dy, w, rope=rope, rope_base=S.ROPE_BASE),
+                       O.premix_bwd_dw(dy, x, pm.P, rope=rope, rope_base=S.ROPE_BASE)),
+              pm.N / ntok)
+    n_all = aw.B * aw.N * aw.HP
+    n = max(1, int(n_all * frac))
+    timed(lambda: attn_rows(host["a_q"], host["a_k"], host["a_v"], aw.HP, aw.N, aw.B,
+                            O.MASK_CAUSAL_WINDOW, S.WINDOW_KEYS, n), n_all / n)
     nb = max(1, int(mu.B * frac))
     x, keep = host["mu_x"][:nb], host["mu_keep"][:nb]
-    t0 = time.perf_counter()
-    gg = O.mu_gather(x, keep, mu.grid_h, mu.grid_w, mu.mu_h, mu.mu_w)
-    u = gg.reshape(nb * mu.n_keep, 1, mu.unit_tokens, 1, mu.C)
-    ou, _ = O.attention(u, u, u)
-    ob = S.f32_to_bf16_bits(ou.astype(np.float32)).reshape(nb, mu.n_keep, mu.unit_tokens, mu.C)
-    O.mu_scatter(ob, keep, np.zeros_like(x), mu.grid_h, mu.grid_w, mu.mu_h, mu.mu_w)
-    t_total += (time.perf_counter() - t0) * (mu.B / nb)
-    desc = (f"{ntok}/{pm.N} tokens per premix op, {nrows}/{nrows_all} attention rows, "
-            f"{nb}/{mu.B} Hiera samples; times scaled to the full step")
-    return t_total, desc, O.num_threads()
+
+    def hiera():
+        gg = O.mu_gather(x, keep, mu.grid_h, mu.grid_w, mu.mu_h, mu.mu_w)
+        u = gg.reshape(nb * mu.n_keep, 1, mu.unit_tokens, 1, mu.C)
+        ou, _ = O.attention(u, u, u)
+        ob = S.f32_to_bf16_bits(ou.astype(np.float32)).reshape(nb, mu.n_keep, mu.unit_tokens,
+                                                               mu.C)
+        O.mu_scatter(ob, keep, np.zeros_like(x), mu.grid_h, mu.grid_w, mu.mu_h, mu.mu_w)
+
+    timed(hiera, mu.B / nb)
+    ntok = max(1, int(lc.N * frac))
+    ys = {}
+    for t in "qkv":
+        x, w = host[f"lx_{t}"][:, :ntok], host[f"lw_{t}"]
+
+        def fwd(t=t, x=x, w=w):
+            ys[t] = O.premix_fwd(x, w, lc.P, rope=(t != "v"), rope_base=S.ROPE_BASE)
+
+        timed(fwd, lc.N / ntok)
+    # causal attention rows (independent; a row's cost depends only on its
+    # position, so one head of full-length inputs stands in for all 80)
+    n_all = lc.B * lc.N * lc.HP
+    n = max(1, int(n_all * frac))
+    qa, ka, va = (np.ascontiguousarray(host[f"lx_{t}"][:, :, :1]) for t in "qkv")
+    timed(lambda: attn_rows(qa, ka, va, 1, lc.N, lc.B, O.MASK_CAUSAL, 0, n), n_all / n)
+    desc = (f"random {frac:.5f} of every op: tokens of each premix, query rows of each attention "
+            f"(uniform over batch, head, position), Hiera samples; each op's time scaled by "
+            f"its sampled share")
+    return t_full, t_meas, desc, O.num_threads()
 
 
 def ideal_step_seconds():
     peaks, _ = load_peaks()
-    hbm = peaks["hbm_gbs"] * 1e9
-    tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 1e12
-    return sum(max(b / hbm, (f / tc) if f else 0.0) for _, _, b, f in op_table())
+    hbm, tc = peaks["hbm_gbs"] * 1e9, peaks["bf16_tflops"] * 1e12
+    return sum(max(b / hbm, (f / tc) if f else 0.0) for _, b, f in op_table())
 
 
 def reference_arm(args, rank, world):
@@ -422,37 +520,40 @@ def reference_arm(args, rank, world):
         return None
     host = host_inputs(seed=0)
     ideal = ideal_step_seconds()
-    for _ in range(args.warmup):
-        oracle_sample(host, args.ref_frac)
-    times = []
-    for _ in range(args.steps):
-        t, desc, cores = oracle_sample(host, args.ref_frac)
-        times.append(t)
-    sec = statistics.mean(times)
+    for w in range(args.warmup):
+        oracle_sample(host, args.cpu_frac, seed=1000 + w)
+    full, meas = [], []
+    for s in range(args.steps):
+        f, m, desc, cores = oracle_sample(host, args.cpu_frac, seed=s)
+        full.append(f)
+        meas.append(m)
+    sec = statistics.mean(full)
     val = round(100.0 * ideal / sec, 8)
-    unit = "% of 1-GPU roofline, summed over GPUs"
-    return {"impl": "reference", "metric": METRIC, "value": val, "unit": unit, "n_gpus": world,
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
+            "ms_per_step_kind": "scaled from the sample (see cpu_baseline.sample)",
+            "sample_ms_per_step_measured": round(statistics.mean(meas) * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": "same step as the GPU arm (oracle, CPU)"},
-            "cpu_baseline": {"value": val, "unit": unit, "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": desc},
-            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
 
 # --------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs of the run; must equal WORLD_SIZE (torchrun) when > 1")
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-frac", type=float, default=1 / 4,
-                    help="fraction of the step the CPU baseline samples")
-    ap.add_argument("--ref-frac", type=float, default=1 / 64,
-                    help="fraction of the step each reference-arm step samples")
+    ap.add_argument("--cpu-frac", type=float, default=CPU_FRAC,
+                    help="fraction of every op each oracle sample runs")
+    ap.add_argument("--cpu-samples", type=int, default=2,
+                    help="oracle samples behind the cpu_baseline of the GPU arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -461,6 +562,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N>1 with "
+                 f"torch.distributed.run --nproc-per-node N")
 
     if args.impl == "reference":
         line = reference_arm(args, rank, world)
@@ -468,21 +572,28 @@ def main():
             print(json.dumps(line), flush=True)
         return
 
-    # oracle CPU baseline first (spawned-free: before any CUDA call in this process)
+    # oracle CPU baseline first, before any CUDA call in this process
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = host_inputs(seed=0)
-        sec, desc, cores = oracle_sample(host, args.cpu_frac)
-        cpu = {"value": round(100.0 * ideal_step_seconds() / sec, 8),
-               "unit": "% of 1-GPU roofline, summed over GPUs", "cores": cores, "kind": "oracle",
-               "sample": desc, "ms_per_step": round(sec * 1e3, 1)}
+        full, meas = [], []
+        for s in range(args.cpu_samples):
+            f, m, desc, cores = oracle_sample(host, args.cpu_frac, seed=s)
+            full.append(f)
+            meas.append(m)
+        sec = statistics.mean(full)
+        cpu = {"value": round(100.0 * ideal_step_seconds() / sec, 8), "unit": UNIT,
+               "cores": cores, "kind": "oracle", "sample": desc,
+               "ms_per_step_scaled": round(sec * 1e3, 1),
+               "sample_ms_measured": round(statistics.mean(meas) * 1e3, 1),
+               "samples": args.cpu_samples}
         del host
 
     if world > 1:
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    line, _ = gpu_arm(args, rank, world, local_rank)
+    line = gpu_arm(args, rank, world, local_rank)
     line["cpu_baseline"] = cpu
     if world > 1:
         import torch

@@ -172,6 +172,20 @@ iha_status mu_scatter(const void* src, const int32_t* keep, void* x, int B,
                       int grid_h, int grid_w, int mu_h, int mu_w, int n_keep,
                       int C, int elem_bytes, void* stream);
 
+/*
+ * Test hook for the failure path; never needed in normal use.  Arms the next
+ * bf16 mha_fwd launch made on the calling host thread (one shot) so that
+ * CTA 0 withholds the load of its first V tile and every wait of that launch
+ * gives up after limit_us microseconds (1 .. 1e6) instead of the normal 4 s.
+ * The launch then takes its abort path: the waiting role raises the block's
+ * abort flag, the others unwind, TMA copies in flight land, the MMAs drain,
+ * tensor memory is released, and the kernel returns with device error 2
+ * (iha_device_error); the rows of CTA 0's work are left unwritten.  The GPU
+ * context stays usable and the next launch runs normally.
+ * IHA_ERR_INVALID_ARG for a limit out of range.
+ */
+iha_status iha_test_fail_next_wait(int limit_us);
+
 /* Static description of a status code. */
 const char* iha_status_string(iha_status status);
 

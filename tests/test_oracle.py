@@ -340,3 +340,77 @@ def test_keep_units_sorted_unique():
     assert keep.shape == (128, 20)
     for row in keep:
         assert list(row) == sorted(set(row.tolist())) and 0 <= row.min() and row.max() < 49
+
+
+# ----------------------------------------------------------------- bf16 rounding
+def test_round_bf16_hand_ties():
+    """Round-to-nearest-even onto the bf16 grid (8 significand bits): values
+    between two neighbours go to the nearer one; exact halves go to the one
+    with an even last significand bit."""
+    u = 2.0 ** -7                       # bf16 ulp on [1, 2)
+    cases = [
+        (1.0, 1.0),
+        (1.0 + u / 2, 1.0),             # tie, 1.0 is even -> stays
+        (1.0 + 3 * u / 2, 1.0 + 2 * u),  # tie between odd 1+u and even 1+2u
+        (1.0 + u / 2 + 2.0 ** -20, 1.0 + u),  # just above the tie -> up
+        (1.0 + u / 2 - 2.0 ** -20, 1.0),      # just below the tie -> down
+        (-(1.0 + 3 * u / 2), -(1.0 + 2 * u)),  # sign symmetric
+        (3.0 + 2.0 ** -7, 3.0),         # ulp on [2, 4) is 2^-6: tie, 3.0 even
+        (0.0, 0.0),
+        (2.0 ** -130, 2.0 ** -130),     # subnormal with few bits is exact
+        (255.5, 256.0),                 # ulp 1 on [128, 256): tie to even 256
+        (254.5, 254.0),                 # tie to even 254
+        (1e30, None),                   # large value, checked by bits below
+    ]
+    got = O.round_bf16(np.array([c[0] for c in cases]))
+    for (x, want), g in zip(cases[:-1], got[:-1]):
+        assert g == want, (x, g, want)
+    # 1e30: checked against the bit pattern rounded by hand (no tie)
+    f = int(np.array(1e30, np.float32).view(np.uint32))
+    want = np.array((f + 0x8000) & 0xFFFF0000, np.uint32).view(np.float32)
+    assert got[-1] == float(want)
+
+
+def test_round_bf16_matches_torch_cast():
+    """Cross-check on random values against torch's own float32 -> bfloat16 cast."""
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(7)
+    x = np.concatenate([g.standard_normal(20000) * 10.0 ** g.integers(-20, 20, 20000),
+                        np.float32(1.0) + np.arange(512) * 2.0 ** -9]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_bf16(x.astype(np.float64)), ref)
+
+
+# ----------------------------------------------------------------- RoPE position offset
+@pytest.mark.parametrize("n0", [1, 5, 13])
+def test_premix_pos0_window_equals_slice_of_full_sequence(n0):
+    """A window starting at row n0 with pos0 = n0 reproduces rows n0.. of the
+    whole-sequence result exactly (forward and input gradient)."""
+    B, N, H, P, d = 2, 17, 3, 2, 16
+    x = S.normal((B, N, H, d), 31, 0, dtype="f32")
+    dy = S.normal((B, N, H * P, d), 31, 1, dtype="f32")
+    w = S.premix_weight(H, P, 31, 2)
+    full = O.premix_fwd(x, w, P, rope=True, rope_base=50.0)
+    win = O.premix_fwd(np.ascontiguousarray(x[:, n0:]), w, P, rope=True, rope_base=50.0, pos0=n0)
+    np.testing.assert_array_equal(win, full[:, n0:])
+    fdx = O.premix_bwd_dx(dy, w, rope=True, rope_base=50.0)
+    wdx = O.premix_bwd_dx(np.ascontiguousarray(dy[:, n0:]), w, rope=True, rope_base=50.0, pos0=n0)
+    np.testing.assert_array_equal(wdx, fdx[:, n0:])
+    # and without the offset the window would be rotated by the wrong angles
+    wrong = O.premix_fwd(np.ascontiguousarray(x[:, n0:]), w, P, rope=True, rope_base=50.0)
+    assert not np.allclose(wrong[:, 1:], full[:, n0 + 1:])
+
+
+def test_premix_pos0_rotates_by_absolute_position():
+    """pos0 = n0 equals the plain mix followed by RoPE at positions n0 + row,
+    built from the d = 2 closed form (rotation by n radians when base^0 = 1)."""
+    B, N, H, P, n0 = 1, 4, 2, 1, 6
+    x = S.normal((B, N, H, 2), 32, 0, dtype="f32")
+    w = S.premix_weight(H, P, 32, 1)
+    y = O.premix_fwd(x, w, P, rope=True, rope_base=7.0, pos0=n0)
+    m = O.premix_fwd(x, w, P)
+    for n in range(N):
+        c, s = math.cos(n0 + n), math.sin(n0 + n)
+        a, b = m[0, n, :, 0], m[0, n, :, 1]
+        np.testing.assert_allclose(y[0, n, :, 0], a * c - b * s, atol=1e-12)
+        np.testing.assert_allclose(y[0, n, :, 1], b * c + a * s, atol=1e-12)

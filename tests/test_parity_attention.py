@@ -71,6 +71,27 @@ def test_attention_bf16_small(T, case):
     assert T.device_error() == 0
 
 
+# Several work items per persistent CTA (more items than SMs), an odd number
+# of query tiles (the last item has one tile), heads spread over groups.
+MANY_ITEM_CASES = [  # (B, N, Hh, d, mask, window)
+    (2, 1030, 48, 128, O.MASK_CAUSAL_WINDOW, 300),
+    (1, 1100, 40, 128, O.MASK_CAUSAL, 0),
+    (3, 390, 64, 64, O.MASK_NONE, 0),
+]
+
+
+@pytest.mark.parametrize("case", MANY_ITEM_CASES)
+def test_attention_bf16_many_items_per_cta(T, case):
+    B, N, Hh, d, mask, window = case
+    q, k, v = _qkv((B, N, Hh, d), (B, N, Hh, d), seed=N + Hh)
+    o, lse = T.mha_fwd(to_dev(q), to_dev(k), to_dev(v), mask=mask, window=window,
+                       return_lse=True)
+    ro, rl = O.attention(q[:, None], k[:, None], v[:, None], mask, window)
+    assert_bf16_close(to_f64(o), ro[:, 0], f"O {case}")
+    _lse_close(to_f64(lse)[:, 0], rl[:, 0], f"lse {case}")
+    assert T.device_error() == 0
+
+
 def test_attention_bf16_nq_ne_nk(T):
     q, _, _ = _qkv((2, 200, 3, 128), (2, 333, 3, 128), seed=7)
     _, k, v = _qkv((2, 333, 3, 128), (2, 333, 3, 128), seed=8)

@@ -10,8 +10,8 @@ import pytest
 
 import oracle as O
 import synthetic as S
-from helpers import (abs_bits, assert_bf16_close, assert_dw_close, assert_f32_close, to_dev,
-                     to_f64)
+from helpers import (assert_bf16_close, assert_dw_close, assert_f32_close, dw_abs_sum, dw_chain,
+                     to_dev, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -22,6 +22,22 @@ SHAPES = [  # (B, N, H, P, d)
     (1, 33, 7, 5, 96),
     (2, 17, 32, 4, 16),
     (1, 3, 1, 1, 8),
+]
+
+# Edges of the tensor-core kernels' range (bf16, d in {64, 128}, H <= 32,
+# H*P <= 128): full M = 128 tiles, padded pseudo-head counts, K = 32 source
+# heads, and small H*P at d = 128 (one or two 16-row K-steps of dY).
+TC_EDGE_SHAPES = [  # (B, N, H, P, d)
+    (1, 19, 24, 4, 128),   # H*P = 96
+    (1, 19, 32, 4, 128),   # H*P = 128, H = 32
+    (1, 23, 16, 8, 128),   # H*P = 128, P = 8
+    (1, 23, 19, 5, 128),   # H*P = 95 (padded to 96), P = 5
+    (2, 11, 24, 5, 64),    # H*P = 120, d = 64
+    (1, 13, 32, 4, 64),    # H*P = 128, d = 64
+    (2, 21, 4, 4, 128),    # H*P = 16
+    (1, 25, 12, 4, 128),   # H*P = 48
+    (1, 9, 4, 2, 128),     # H*P = 8
+    (1, 7, 1, 1, 128),     # H = P = 1
 ]
 
 
@@ -46,26 +62,38 @@ def _rope_ok(d):
     return d >= 16 and d <= 128 and (d & (d - 1)) == 0
 
 
+def _check_all_ops(T, shape, rope, seed, base=100.0):
+    B, N, H, P, d = shape
+    x, dy, w = _inputs(B, N, H, P, d, seed=seed)
+    y = T.premix_fwd(to_dev(x), to_dev(w), P, rope=rope, rope_base=base)
+    assert_bf16_close(to_f64(y), O.premix_fwd(x, w, P, rope=rope, rope_base=base), "fwd")
+    rdx = O.premix_bwd_dx(dy, w, rope=rope, rope_base=base)
+    dx = T.premix_bwd_dx(to_dev(dy), to_dev(w), rope=rope, rope_base=base)
+    assert_bf16_close(to_f64(dx), rdx, "dx")
+    dw = T.premix_bwd_dw(to_dev(dy), to_dev(x), P, rope=rope, rope_base=base)
+    absum = dw_abs_sum(dy, x, P, rope)
+    chain = dw_chain(B, N, H, P, d, rope=rope)
+    rdw = O.premix_bwd_dw(dy, x, P, rope=rope, rope_base=base)
+    assert_dw_close(to_f64(dw), rdw, absum, chain, rope, "dw")
+    # both gradients from one pass over dY
+    dx2, dw2 = T.premix_bwd(to_dev(dy), to_dev(x), to_dev(w), rope=rope, rope_base=base)
+    assert_bf16_close(to_f64(dx2), rdx, "fused dx")
+    assert_dw_close(to_f64(dw2), rdw, absum, chain, rope, "fused dw")
+    assert T.device_error() == 0
+
+
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("rope", [False, True])
 def test_premix_bf16_small(T, shape, rope):
-    B, N, H, P, d = shape
-    if rope and not _rope_ok(d):
+    if rope and not _rope_ok(shape[4]):
         pytest.skip("RoPE needs d a power of two")
-    x, dy, w = _inputs(B, N, H, P, d, seed=11 + d)
-    base = 100.0
-    y = T.premix_fwd(to_dev(x), to_dev(w), P, rope=rope, rope_base=base)
-    assert_bf16_close(to_f64(y), O.premix_fwd(x, w, P, rope=rope, rope_base=base), "fwd")
-    dx = T.premix_bwd_dx(to_dev(dy), to_dev(w), rope=rope, rope_base=base)
-    assert_bf16_close(to_f64(dx), O.premix_bwd_dx(dy, w, rope=rope, rope_base=base), "dx")
-    dw = T.premix_bwd_dw(to_dev(dy), to_dev(x), P, rope=rope, rope_base=base)
-    absum = O.premix_bwd_dw(abs_bits(dy), abs_bits(x), P) * (2.0 if rope else 1.0)
-    rdw = O.premix_bwd_dw(dy, x, P, rope=rope, rope_base=base)
-    assert_dw_close(to_f64(dw), rdw, absum, "dw")
-    # both gradients from one pass over dY
-    dx2, dw2 = T.premix_bwd(to_dev(dy), to_dev(x), to_dev(w), rope=rope, rope_base=base)
-    assert_bf16_close(to_f64(dx2), O.premix_bwd_dx(dy, w, rope=rope, rope_base=base), "fused dx")
-    assert_dw_close(to_f64(dw2), rdw, absum, "fused dw")
+    _check_all_ops(T, shape, rope, seed=11 + shape[4])
+
+
+@pytest.mark.parametrize("shape", TC_EDGE_SHAPES)
+@pytest.mark.parametrize("rope", [False, True])
+def test_premix_bf16_tensor_core_edges(T, shape, rope):
+    _check_all_ops(T, shape, rope, seed=3 + shape[2] * shape[3])
 
 
 @pytest.mark.parametrize("rope", [False, True])
@@ -95,15 +123,16 @@ def test_premix_llama_shape_sampled(T):
         assert_bf16_close(y[:, sl], O.premix_fwd(x[:, sl], w, sh.P), f"fwd@{n0}")
         assert_bf16_close(dx[:, sl], O.premix_bwd_dx(dy[:, sl], w), f"dx@{n0}")
     dw = to_f64(T.premix_bwd_dw(to_dev(dy), to_dev(x), sh.P))
-    absum = O.premix_bwd_dw(abs_bits(dy), abs_bits(x), sh.P)
+    absum = dw_abs_sum(dy, x, sh.P)
+    chain = dw_chain(sh.B, sh.N, sh.H, sh.P, sh.d)
     rdw = O.premix_bwd_dw(dy, x, sh.P)
-    assert_dw_close(dw, rdw, absum, "dw full")
+    assert_dw_close(dw, rdw, absum, chain, False, "dw full")
     dx2, dw2 = T.premix_bwd(to_dev(dy), to_dev(x), to_dev(w))
     dx2 = to_f64(dx2)
     for n0 in (0, sh.N - 131):
         sl = slice(n0, n0 + 131)
         assert_bf16_close(dx2[:, sl], O.premix_bwd_dx(dy[:, sl], w), f"fused dx@{n0}")
-    assert_dw_close(to_f64(dw2), rdw, absum, "fused dw full")
+    assert_dw_close(to_f64(dw2), rdw, absum, chain, False, "fused dw full")
 
 
 def test_premix_long_context_rope_sampled(T):
@@ -127,9 +156,9 @@ def test_premix_long_context_rope_sampled(T):
         assert_bf16_close(dx[:, sl], ref, f"dx rope@{n0}")
         assert_bf16_close(dx2[:, sl], ref, f"fused dx rope@{n0}")
     # dW with RoPE at this size: the full oracle reduction over 32768 tokens
-    absum = 2.0 * O.premix_bwd_dw(abs_bits(dy), abs_bits(x), sh.P)
     assert_dw_close(to_f64(dw2), O.premix_bwd_dw(dy, x, sh.P, rope=True, rope_base=S.ROPE_BASE),
-                    absum, "fused dw rope")
+                    dw_abs_sum(dy, x, sh.P, True), dw_chain(sh.B, sh.N, sh.H, sh.P, sh.d, rope=True),
+                    True, "fused dw rope")
 
 
 def test_premix_one_hot_copies_are_bit_exact(T):

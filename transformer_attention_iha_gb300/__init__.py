@@ -31,7 +31,7 @@ MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW = 0, 1, 2
 
 SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",
            "mha_fwd", "mu_gather", "mu_scatter", "iha_status_string", "iha_last_error",
-           "iha_device_error")
+           "iha_device_error", "iha_test_fail_next_wait")
 
 
 class IHAError(RuntimeError):
@@ -80,6 +80,8 @@ def lib() -> C.CDLL:
     L.iha_last_error.restype = C.c_char_p
     L.iha_device_error.argtypes = [i]
     L.iha_device_error.restype = C.c_int
+    L.iha_test_fail_next_wait.argtypes = [i]
+    L.iha_test_fail_next_wait.restype = C.c_int
     _lib = L
     return L
 
@@ -128,15 +130,33 @@ def _need_cuda(*ts):
             raise ValueError("tensors must live on a CUDA device")
 
 
+def _expect(t, name: str, shape=None, dtype=None, device=None, contiguous: bool = True):
+    """Host-side argument check: raises before anything reaches the library."""
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must live on a CUDA device")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
 # ---------------------------------------------------------------- premix
 def premix_fwd(x, w, P: int, rope: bool = False, rope_base: float = 10000.0, out=None,
                stream=None):
     """Y[B,N,H*P,d] = premix of X[B,N,H,d] with W[H,P,H] (fp32), optional RoPE."""
     torch = _torch()
-    _need_cuda(x, w)
+    _expect(x, "x")
+    if x.dim() != 4:
+        raise ValueError("x must be [B, N, H, d]")
     B, N, H, d = x.shape
+    _expect(w, "w", (H, P, H), torch.float32, x.device)
     if out is None:
         out = torch.empty((B, N, H * P, d), dtype=x.dtype, device=x.device)
+    _expect(out, "out", (B, N, H * P, d), x.dtype, x.device)
     check(lib().iha_premix_fwd(_ptr(x), _ptr(w), _ptr(out), B, N, H, P, d, _dt(x), int(rope),
                                float(rope_base), _stream(stream)), "iha_premix_fwd")
     return out
@@ -146,11 +166,17 @@ def premix_bwd_dx(dy, w, rope: bool = False, rope_base: float = 10000.0, out=Non
                   stream=None):
     """dX[B,N,H,d] = W^T dY (with the inverse RoPE when rope)."""
     torch = _torch()
-    _need_cuda(dy, w)
-    B, N, HP, d = dy.shape
+    _expect(w, "w", dtype=torch.float32)
+    if w.dim() != 3 or w.shape[0] != w.shape[2]:
+        raise ValueError("w must be [H, P, H]")
     H, P, _ = w.shape
+    _expect(dy, "dy", device=w.device)
+    if dy.dim() != 4 or dy.shape[2] != H * P:
+        raise ValueError(f"dy must be [B, N, H*P={H * P}, d], got {tuple(dy.shape)}")
+    B, N, _, d = dy.shape
     if out is None:
         out = torch.empty((B, N, H, d), dtype=dy.dtype, device=dy.device)
+    _expect(out, "out", (B, N, H, d), dy.dtype, dy.device)
     check(lib().iha_premix_bwd_dx(_ptr(dy), _ptr(w), _ptr(out), B, N, H, P, d, _dt(dy),
                                   int(rope), float(rope_base), _stream(stream)),
           "iha_premix_bwd_dx")
@@ -161,10 +187,14 @@ def premix_bwd_dw(dy, x, P: int, rope: bool = False, rope_base: float = 10000.0,
                   stream=None):
     """dW[H,P,H] (fp32, overwritten) = sum over tokens and features of dY X^T."""
     torch = _torch()
-    _need_cuda(dy, x)
+    _expect(x, "x")
+    if x.dim() != 4:
+        raise ValueError("x must be [B, N, H, d]")
     B, N, H, d = x.shape
+    _expect(dy, "dy", (B, N, H * P, d), x.dtype, x.device)
     if out is None:
         out = torch.empty((H, P, H), dtype=torch.float32, device=x.device)
+    _expect(out, "out", (H, P, H), torch.float32, x.device)
     check(lib().iha_premix_bwd_dw(_ptr(dy), _ptr(x), _ptr(out), B, N, H, P, d, _dt(x),
                                   int(rope), float(rope_base), _stream(stream)),
           "iha_premix_bwd_dw")
@@ -175,13 +205,21 @@ def premix_bwd(dy, x, w, rope: bool = False, rope_base: float = 10000.0, dx=None
                stream=None):
     """(dX, dW) in one pass over dY: dX = W^T dY (inverse RoPE when rope), dW = sum dY X^T."""
     torch = _torch()
-    _need_cuda(dy, x, w)
+    _expect(x, "x")
+    if x.dim() != 4:
+        raise ValueError("x must be [B, N, H, d]")
     B, N, H, d = x.shape
+    if w.dim() != 3:
+        raise ValueError("w must be [H, P, H]")
     P = w.shape[1]
+    _expect(w, "w", (H, P, H), torch.float32, x.device)
+    _expect(dy, "dy", (B, N, H * P, d), x.dtype, x.device)
     if dx is None:
         dx = torch.empty_like(x)
     if dw is None:
         dw = torch.empty((H, P, H), dtype=torch.float32, device=x.device)
+    _expect(dx, "dx", (B, N, H, d), x.dtype, x.device)
+    _expect(dw, "dw", (H, P, H), torch.float32, x.device)
     check(lib().iha_premix_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(dx), _ptr(dw), B, N, H, P, d,
                                _dt(x), int(rope), float(rope_base), _stream(stream)),
           "iha_premix_bwd")
@@ -213,15 +251,25 @@ def mha_fwd(q, k, v, mask: int = MASK_NONE, window: int = 0, scale: float = 0.0,
     also lse [Bo, Bi, Hh, Nq] fp32 (natural log, scale included).
     """
     torch = _torch()
-    _need_cuda(q, k, v)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _expect(t, name, dtype=q.dtype, device=q.device, contiguous=False)
     q5, k5, v5 = _as5(q), _as5(k), _as5(v)
     Bo, Bi, Nq, Hh, d = q5.shape
     Nk = k5.shape[2]
+    if tuple(k5.shape) != (Bo, Bi, Nk, Hh, d) or tuple(v5.shape) != (Bo, Bi, Nk, Hh, d):
+        raise ValueError(f"k {tuple(k5.shape)} / v {tuple(v5.shape)} do not match q "
+                         f"{tuple(q5.shape)}")
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    _expect(out, "out", q.shape, q.dtype, q.device, contiguous=False)
     o5 = _as5(out)
     if lse is None and return_lse:
         lse = torch.empty((Bo, Bi, Hh, Nq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        if lse.numel() != Bo * Bi * Hh * Nq:
+            raise ValueError(f"lse: {lse.numel()} elements, expected [Bo, Bi, Hh, Nq] = "
+                             f"{(Bo, Bi, Hh, Nq)}")
+        _expect(lse, "lse", dtype=torch.float32, device=q.device)
     check(lib().mha_fwd(_ptr(q5), _ptr(k5), _ptr(v5), _ptr(o5),
                         C.c_void_p(lse.data_ptr() if lse is not None else 0), Bo, Bi, Hh, Nq,
                         Nk, d, _strides(q5), _strides(k5), _strides(v5), _strides(o5),
@@ -231,14 +279,26 @@ def mha_fwd(q, k, v, mask: int = MASK_NONE, window: int = 0, scale: float = 0.0,
 
 
 # ---------------------------------------------------------------- gather / scatter
+def _mu_check(x, keep, grid_h: int, grid_w: int, mu_h: int, mu_w: int):
+    torch = _torch()
+    _expect(x, "x")
+    if x.dim() != 3 or x.shape[1] != grid_h * grid_w:
+        raise ValueError(f"x must be [B, grid_h*grid_w={grid_h * grid_w}, C], got "
+                         f"{tuple(x.shape)}")
+    _expect(keep, "keep", dtype=torch.int32, device=x.device)
+    if keep.dim() != 2 or keep.shape[0] != x.shape[0]:
+        raise ValueError(f"keep must be [B={x.shape[0]}, n_keep] int32, got {tuple(keep.shape)}")
+
+
 def mu_gather(x, keep, grid_h: int, grid_w: int, mu_h: int, mu_w: int, out=None, stream=None):
     """x [B, grid_h*grid_w, C] -> [B, n_keep, mu_h*mu_w, C] (bit-exact copy)."""
     torch = _torch()
-    _need_cuda(x, keep)
+    _mu_check(x, keep, grid_h, grid_w, mu_h, mu_w)
     B, G, Cc = x.shape
     n_keep = keep.shape[1]
     if out is None:
         out = torch.empty((B, n_keep, mu_h * mu_w, Cc), dtype=x.dtype, device=x.device)
+    _expect(out, "out", (B, n_keep, mu_h * mu_w, Cc), x.dtype, x.device)
     check(lib().mu_gather(_ptr(x), _ptr(keep), _ptr(out), B, grid_h, grid_w, mu_h, mu_w, n_keep,
                           Cc, x.element_size(), _stream(stream)), "mu_gather")
     return out
@@ -246,9 +306,10 @@ def mu_gather(x, keep, grid_h: int, grid_w: int, mu_h: int, mu_w: int, out=None,
 
 def mu_scatter(src, keep, x, grid_h: int, grid_w: int, mu_h: int, mu_w: int, stream=None):
     """In place: x[b, tok(keep[b,k], t), :] = src[b, k, t, :]."""
-    _need_cuda(src, keep, x)
+    _mu_check(x, keep, grid_h, grid_w, mu_h, mu_w)
     B, G, Cc = x.shape
     n_keep = keep.shape[1]
+    _expect(src, "src", (B, n_keep, mu_h * mu_w, Cc), x.dtype, x.device)
     check(lib().mu_scatter(_ptr(src), _ptr(keep), _ptr(x), B, grid_h, grid_w, mu_h, mu_w, n_keep,
                            Cc, x.element_size(), _stream(stream)), "mu_scatter")
     return x

@@ -12,6 +12,9 @@ namespace iha {
 
 namespace {
 thread_local char t_last_error[512] = "";
+// One-shot failure-path test (iha_test_fail_next_wait): 0 = not armed.
+thread_local uint64_t t_test_limit_ns = 0;
+thread_local bool t_test_withhold = false;
 std::mutex g_reader_mu;
 dev_error_reader g_readers[16];
 int g_n_readers = 0;
@@ -30,6 +33,18 @@ iha_status check_launch(const char* what) {
   if (e != cudaSuccess)
     return fail(IHA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return IHA_OK;
+}
+
+uint64_t wait_limit_for_next_launch() {
+  const uint64_t v = t_test_limit_ns;
+  t_test_limit_ns = 0;
+  return v ? v : kWaitLimitNs;
+}
+
+bool withhold_for_this_launch() {
+  const bool v = t_test_withhold;
+  t_test_withhold = false;
+  return v;
 }
 
 int register_dev_error_reader(dev_error_reader r) {
@@ -87,6 +102,14 @@ const char* iha_status_string(iha_status s) {
 }
 
 const char* iha_last_error(void) { return iha::t_last_error; }
+
+iha_status iha_test_fail_next_wait(int limit_us) {
+  if (limit_us < 1 || limit_us > 1000000)
+    return iha::fail(IHA_ERR_INVALID_ARG, "iha_test_fail_next_wait: limit_us must be in [1, 1e6]");
+  iha::t_test_limit_ns = (uint64_t)limit_us * 1000ull;
+  iha::t_test_withhold = true;
+  return IHA_OK;
+}
 
 int iha_device_error(int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return -1;

@@ -7,23 +7,32 @@
 // MaskUnitAttentionFast.forward (unmasked attention inside each mask unit,
 // scale head_dim ** -0.5, tokens laid out (T outer, units inner)).
 //
-// bf16 path (sm_103a tensor cores):
-//   CTA = two 128-row query tiles of one head (256 rows), 10 warps:
-//     warps 0-3  softmax of query tile 0 (thread = row = TMEM lane)
-//     warps 4-7  softmax of query tile 1
-//     warp  8    TMA producer: Q once, then K / V tiles into a 2-stage ring
+// bf16 path (sm_103a tensor cores), persistent:
+//   One CTA per SM walks a static list of work items; an item is two
+//   adjacent 128-row query tiles of one head.  Items are grouped by heads
+//   (a group's K / V stays in L2 while its items run) and, inside a group,
+//   ordered heaviest first (longest key range), dealt round-robin to CTAs.
+//   10 warps:
+//     warps 0-3  softmax + epilogue of query tile 0 (thread = row = TMEM lane)
+//     warps 4-7  softmax + epilogue of query tile 1
+//     warp  8    TMA producer: Q tiles per item, K and V tiles into separate
+//                two-slot rings (a K slot frees after its QK^T, a V slot
+//                after its P.V, so K runs ahead of V)
 //     warp  9    tcgen05.mma issuer (one thread) and TMEM owner
 //   TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  P (bf16)
 //   overwrites the first 64 columns of S and feeds the P.V MMA as the
 //   A operand straight from tensor memory.
+//   Each query tile visits only its own key-tile range (causal / window
+//   block skipping); the two tiles of an item share the K / V stream.
 //   Online softmax in the log2 domain with conditional rescaling: O and l
 //   are rescaled only when a row maximum grows by more than 8 (a factor of
 //   256), which keeps every exponent <= 2^8 and is exact in real arithmetic.
-//   KV tiles outside the causal / window band of the query-tile pair are
-//   never loaded (block skipping); tiles crossing a band edge or the key
-//   tail are masked element-wise.
+//   A quarter of the exponentials run as a polynomial on the FMA pipe so the
+//   MUFU unit does not bound the softmax.
 // f32 path: CUDA-core kernel in fp32 throughout (no TF32), for fp32 tensors.
 #include <math.h>
+
+#include <mutex>
 
 #include "common.cuh"
 
@@ -40,28 +49,72 @@ constexpr int kThreads = 320;
 constexpr int kSmemTiles = 12 * kTileChunkBytes;  // Q 2x2, K 2x2, V 2x2 chunks
 constexpr int kSmemBytes = kSmemTiles + 256 + 1024;  // + barriers + alignment slack
 constexpr float kRescaleLog2 = 8.0f;
+// L2 budget for the K / V of one head group.
+constexpr int64_t kGroupKVBytes = 48ll << 20;
 
 struct AttnParams {
   int Bo, Bi, Hh, Nq, Nk, d, nD;
   int mask, window;
-  int n_qpairs;
+  int n_qt, n_qpairs, n_hb, group, n_items;
   float scale_log2;
   int64_t so_bo, so_bi, so_seq, so_h;
   __nv_bfloat16* o;
   float* lse;
+  uint64_t wait_limit_ns;
+  int withhold;  // failure-path test: CTA 0 never loads its first V tile
 };
 
-// KV tile range [lo, hi] (inclusive) visited by query rows [q_lo, q_hi].
-__device__ __forceinline__ void kv_tile_range(const AttnParams& p, int q_lo, int q_hi, int& lo,
-                                              int& hi) {
+struct Item {
+  int h, bo, bi, bz;
+  int qt0;          // query tiles qt0 and qt0 + 1 (the second only if act1)
+  bool act1;
+  int lo0, hi0;     // key-tile range of query tile qt0 (inclusive)
+  int lo1, hi1;     // ... of query tile qt0 + 1 (empty unless act1)
+  int jlo, jhi;     // union
+};
+
+// KV tile range [lo, hi] (inclusive) of query tile qt.
+__device__ __forceinline__ void kv_tile_range(const AttnParams& p, int qt, int& lo, int& hi) {
   const int n_kt = (p.Nk + kBN - 1) / kBN;
   if (p.mask == IHA_MASK_NONE) {
     lo = 0;
     hi = n_kt - 1;
     return;
   }
+  const int q_lo = qt * kBM, q_hi = min(q_lo + kBM - 1, p.Nq - 1);
   hi = min(q_hi / kBN, n_kt - 1);
   lo = (p.mask == IHA_MASK_CAUSAL_WINDOW) ? max(0, q_lo - (p.window - 1)) / kBN : 0;
+}
+
+// Work item idx: head groups of p.group heads (hb = bz * Hh + h); inside a
+// group, query-tile pairs from the heaviest (latest) down, heads innermost.
+__device__ __forceinline__ Item decode_item(const AttnParams& p, int idx) {
+  const int per_group = p.group * p.n_qpairs;
+  const int n_groups = (p.n_hb + p.group - 1) / p.group;
+  const int g = min(idx / per_group, n_groups - 1);
+  const int hb0 = g * p.group;
+  const int gs = min(p.group, p.n_hb - hb0);
+  const int r = idx - g * per_group;
+  const int rank = r / gs;
+  const int hb = hb0 + (r - rank * gs);
+  Item it;
+  it.h = hb % p.Hh;
+  it.bz = hb / p.Hh;
+  it.bo = it.bz / p.Bi;
+  it.bi = it.bz - it.bo * p.Bi;
+  const int pair = p.n_qpairs - 1 - rank;
+  it.qt0 = 2 * pair;
+  it.act1 = it.qt0 + 1 < p.n_qt;
+  kv_tile_range(p, it.qt0, it.lo0, it.hi0);
+  if (it.act1) {
+    kv_tile_range(p, it.qt0 + 1, it.lo1, it.hi1);
+  } else {
+    it.lo1 = it.lo0;
+    it.hi1 = it.lo0 - 1;  // empty
+  }
+  it.jlo = it.lo0;  // lo1 >= lo0 and hi1 >= hi0: tile 1 is the later one
+  it.jhi = it.act1 ? max(it.hi0, it.hi1) : it.hi0;
+  return it;
 }
 
 __device__ __forceinline__ void raise_error(volatile int* abort_flag) {
@@ -69,6 +122,8 @@ __device__ __forceinline__ void raise_error(volatile int* abort_flag) {
   atomicOr(&g_dev_error, DEV_ERR_WAIT_TIMEOUT);
 }
 
+// NCH = head-dim chunks of 64 (d <= 64: 1, d <= 128: 2).
+template <int NCH>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -77,45 +132,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sQ = smem_u32(smem);                       // [tile][chunk]
-  const uint32_t sK = sQ + 4 * kTileChunkBytes;             // [stage][chunk]
-  const uint32_t sV = sK + 4 * kTileChunkBytes;             // [stage][chunk]
+  const uint32_t sK = sQ + 4 * kTileChunkBytes;             // [slot][chunk]
+  const uint32_t sV = sK + 4 * kTileChunkBytes;             // [slot][chunk]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemTiles);
   const uint32_t bar0 = smem_u32(bars);
-  // barrier slots
-  const uint32_t b_q = bar0;
-  auto b_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto b_vfull = [&](int s) { return bar0 + 8u * (3 + s); };
-  auto b_kvempty = [&](int s) { return bar0 + 8u * (5 + s); };
-  auto b_sfull = [&](int t) { return bar0 + 8u * (7 + t); };
-  auto b_pfull = [&](int t) { return bar0 + 8u * (9 + t); };
-  auto b_ofull = [&](int t) { return bar0 + 8u * (11 + t); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  auto b_qfull = [&](int t) { return bar0 + 8u * (0 + t); };
+  auto b_qempty = [&](int t) { return bar0 + 8u * (2 + t); };
+  auto b_kfull = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto b_kempty = [&](int s) { return bar0 + 8u * (6 + s); };
+  auto b_vfull = [&](int s) { return bar0 + 8u * (8 + s); };
+  auto b_vempty = [&](int s) { return bar0 + 8u * (10 + s); };
+  auto b_sfull = [&](int t) { return bar0 + 8u * (12 + t); };
+  auto b_pfull = [&](int t) { return bar0 + 8u * (14 + t); };
+  auto b_ofull = [&](int t) { return bar0 + 8u * (16 + t); };
+  const uint32_t b_drain = bar0 + 8u * 18;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x;
-  const int bz = blockIdx.y;
-  const int bo = bz / p.Bi, bi = bz - bo * p.Bi;
-  const int pair = p.n_qpairs - 1 - (int)blockIdx.z;  // heaviest (latest) pairs first
-  const int n_qt = (p.Nq + kBM - 1) / kBM;
-  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
-  const bool act1 = qt1 < n_qt;
-  const int q_lo = qt0 * kBM;
-  const int q_hi = min((act1 ? qt1 : qt0) * kBM + kBM - 1, p.Nq - 1);
-  int j_lo, j_hi;
-  kv_tile_range(p, q_lo, q_hi, j_lo, j_hi);
-  const int n_kv = j_hi - j_lo + 1;
+  const uint64_t lim = p.wait_limit_ns;
+  constexpr uint32_t kChunkBytes = (uint32_t)NCH * kTileChunkBytes;
 
   if (threadIdx.x == 0) {
-    mbar_init(b_q, 1);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(b_qfull(s), 1);
+      mbar_init(b_qempty(s), 1);
       mbar_init(b_kfull(s), 1);
+      mbar_init(b_kempty(s), 1);
       mbar_init(b_vfull(s), 1);
-      mbar_init(b_kvempty(s), 1);
+      mbar_init(b_vempty(s), 1);
       mbar_init(b_sfull(s), 1);
       mbar_init(b_pfull(s), 128);
       mbar_init(b_ofull(s), 1);
     }
+    mbar_init(b_drain, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -127,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t chunk_bytes = (uint32_t)p.nD * kTileChunkBytes;
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -135,231 +184,324 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(b_q, (act1 ? 2u : 1u) * chunk_bytes);
-      for (int c = 0; c < p.nD; ++c) {
-        tma_load_5d(sQ + c * kTileChunkBytes, &tmQ, b_q, c * kChunk, qt0 * kBM, h, bi, bo);
-        if (act1)
-          tma_load_5d(sQ + (2 + c) * kTileChunkBytes, &tmQ, b_q, c * kChunk, qt1 * kBM, h, bi, bo);
-      }
-      int issued = 0;
-      for (int it = 0; it < n_kv; ++it) {
-        const int s = it & 1, j = j_lo + it;
-        if (it >= 2 && !mbar_wait(b_kvempty(s), ((it >> 1) - 1) & 1, abort_flag)) {
-          raise_error(abort_flag);
-          break;
+      uint32_t kc = 0, vc = 0, qn0 = 0, qn1 = 0;  // loads issued per ring / Q tile
+      bool ok = true;
+      // Q tile t of item `it` (qn: loads of that tile so far); returns the new count
+      auto load_q = [&](const Item& it, int t, uint32_t qn) -> uint32_t {
+        if (qn > 0 && !(ok = mbar_wait(b_qempty(t), (qn - 1) & 1, abort_flag, lim))) return qn;
+        mbar_arrive_expect_tx(b_qfull(t), kChunkBytes);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+          tma_load_5d(sQ + (2 * t + c) * kTileChunkBytes, &tmQ, b_qfull(t), c * kChunk,
+                      (it.qt0 + t) * kBM, it.h, it.bi, it.bo);
+        return qn + 1;
+      };
+      // load number n of the K (is_v = false) or V ring; returns the new count
+      auto load_kv = [&](const Item& it, int j, bool is_v, uint32_t n) -> uint32_t {
+        const int s = n & 1;
+        if (is_v && n == 0 && p.withhold && blockIdx.x == 0)
+          return n + 1;  // withheld: its consumer's wait runs out (failure-path test)
+        if (n >= 2 && !(ok = mbar_wait(is_v ? b_vempty(s) : b_kempty(s), ((n >> 1) - 1) & 1,
+                                       abort_flag, lim)))
+          return n;
+        const uint32_t full = is_v ? b_vfull(s) : b_kfull(s);
+        mbar_arrive_expect_tx(full, kChunkBytes);
+        const uint32_t dst = (is_v ? sV : sK) + (uint32_t)(2 * s) * kTileChunkBytes;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+          tma_load_5d(dst + c * kTileChunkBytes, is_v ? &tmV : &tmK, full, c * kChunk, j * kBN,
+                      it.h, it.bi, it.bo);
+        return n + 1;
+      };
+      for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+        const Item it = decode_item(p, idx);
+        qn0 = load_q(it, 0, qn0);
+        for (int j = it.jlo; ok && j <= it.jhi; ++j) {
+          kc = load_kv(it, j, false, kc);
+          if (ok && j == it.jlo && it.act1) qn1 = load_q(it, 1, qn1);
+          if (ok) vc = load_kv(it, j, true, vc);
         }
-        mbar_arrive_expect_tx(b_kfull(s), chunk_bytes);
-        for (int c = 0; c < p.nD; ++c)
-          tma_load_5d(sK + (2 * s + c) * kTileChunkBytes, &tmK, b_kfull(s), c * kChunk, j * kBN, h,
-                      bi, bo);
-        mbar_arrive_expect_tx(b_vfull(s), chunk_bytes);
-        for (int c = 0; c < p.nD; ++c)
-          tma_load_5d(sV + (2 * s + c) * kTileChunkBytes, &tmV, b_vfull(s), c * kChunk, j * kBN, h,
-                      bi, bo);
-        issued = it + 1;
       }
-      if (*abort_flag) {
-        // drain: let the copies already in flight land before the CTA exits
-        for (int it = max(0, issued - 2); it < issued; ++it) {
-          const int s = it & 1;
-          volatile int no_abort = 0;
-          mbar_wait(b_kfull(s), (it >> 1) & 1, &no_abort);
-          mbar_wait(b_vfull(s), (it >> 1) & 1, &no_abort);
-        }
-        volatile int no_abort = 0;
-        mbar_wait(b_q, 0, &no_abort);
+      if (!ok) raise_error(abort_flag);
+      // Whoever aborted, no copy may still be landing when the CTA exits: wait
+      // for the last load issued into every slot (in a normal run each has
+      // completed already and the wait returns at once).
+      volatile int no_abort = 0;
+      for (int s = 0; s < 2; ++s) {
+        if (kc > (uint32_t)s)
+          mbar_wait(b_kfull(s), ((kc - 1 - ((kc - 1 - s) & 1)) >> 1) & 1, &no_abort, lim);
+        if (vc > (uint32_t)s)
+          mbar_wait(b_vfull(s), ((vc - 1 - ((vc - 1 - s) & 1)) >> 1) & 1, &no_abort, lim);
       }
+      if (qn0 > 0) mbar_wait(b_qfull(0), (qn0 - 1) & 1, &no_abort, lim);
+      if (qn1 > 0) mbar_wait(b_qfull(1), (qn1 - 1) & 1, &no_abort, lim);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(kBM, p.nD * kChunk, false, true);
-      auto tS = [&](int t) { return tmem + (uint32_t)(t * 128); };
-      auto tO = [&](int t) { return tmem + (uint32_t)(256 + t * 128); };
-      auto issue_qk = [&](int t, int s) {
-        const uint32_t qa = sQ + (uint32_t)(2 * t) * kTileChunkBytes;
-        const uint32_t ka = sK + (uint32_t)(2 * s) * kTileChunkBytes;
-        for (int kk = 0; kk < 4 * p.nD; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kTileChunkBytes + (uint32_t)(kk & 3) * 32u;
-          mma_ss(tS(t), smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                 idesc_qk, kk > 0 ? 1u : 0u);
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, NCH * kChunk, false, true);
+      const uint32_t tS0 = tmem, tS1 = tmem + 128u, tO0 = tmem + 256u, tO1 = tmem + 384u;
+      // descriptors of the chunk-0 / K-step-0 positions; K-step kk of a
+      // 128-byte-swizzled tile adds (kk / 4) * 16 KB + (kk % 4) * 32 B to the
+      // start address, i.e. that >> 4 to the descriptor's low field
+      const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dQ1 = smem_desc_sw128(sQ + 2 * kTileChunkBytes, 16, 1024);
+      const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dK1 = smem_desc_sw128(sK + 2 * kTileChunkBytes, 16, 1024);
+      const uint64_t dV0 = smem_desc_sw128(sV, kTileChunkBytes, 1024);
+      const uint64_t dV1 = smem_desc_sw128(sV + 2 * kTileChunkBytes, kTileChunkBytes, 1024);
+      uint32_t kc = 0, vc = 0, qn0 = 0, qn1 = 0, pn0 = 0, pn1 = 0;
+      bool ok = true;
+      auto issue_qk = [&](uint32_t dS, uint64_t dq, uint32_t kslot) {
+        const uint64_t dk = kslot ? dK1 : dK0;
+#pragma unroll
+        for (int kk = 0; kk < 4 * NCH; ++kk) {
+          const uint64_t off = (uint64_t)(((kk >> 2) * kTileChunkBytes + (kk & 3) * 32) >> 4);
+          mma_ss_nm(dS, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int s, bool acc) {
-        const uint32_t va = sV + (uint32_t)(2 * s) * kTileChunkBytes;
+      auto issue_pv = [&](uint32_t dO, uint32_t aP, uint32_t vslot, uint32_t first) {
+        const uint64_t dv = vslot ? dV1 : dV0;
+#pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tO(t), tS(t) + (uint32_t)(kk * 8), smem_desc_sw128(va + kk * 2048u, kTileChunkBytes, 1024),
-                 idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          mma_ts_nm(dO, aP + (uint32_t)(kk * 8), dv + (uint64_t)(kk * 128), idesc_pv,
+                    (kk > 0 || !first) ? 1u : 0u);
       };
-      bool ok = mbar_wait(b_q, 0, abort_flag) && mbar_wait(b_kfull(0), 0, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(0, 0);
-        mma_commit(b_sfull(0));
-        if (act1) {
-          issue_qk(1, 0);
-          mma_commit(b_sfull(1));
-        }
-      }
-      for (int it = 0; ok && it < n_kv; ++it) {
-        const int s = it & 1;
-        const bool more = it + 1 < n_kv;
-        const int s2 = (it + 1) & 1;
-        if (!(ok = mbar_wait(b_vfull(s), (it >> 1) & 1, abort_flag))) break;
-        if (!(ok = mbar_wait(b_pfull(0), it & 1, abort_flag))) break;
-        tc_fence_after();
-        issue_pv(0, s, it > 0);
-        if (more) {
-          if (!(ok = mbar_wait(b_kfull(s2), ((it + 1) >> 1) & 1, abort_flag))) break;
+      for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+        const Item it = decode_item(p, idx);
+        const uint32_t kbase = kc, vbase = vc;
+        uint32_t k_ready = 0;  // K tiles of this item known to be loaded
+        auto wait_k = [&](int j) {
+          const uint32_t q = (uint32_t)(j - it.jlo);
+          while (ok && k_ready <= q) {
+            const uint32_t n = kbase + k_ready;
+            ok = mbar_wait(b_kfull(n & 1), (n >> 1) & 1, abort_flag, lim);
+            ++k_ready;
+          }
+          return ok;
+        };
+        // prologue: first QK^T of each tile
+        if ((ok = mbar_wait(b_qfull(0), qn0 & 1, abort_flag, lim)) && wait_k(it.lo0)) {
+          ++qn0;
           tc_fence_after();
-          issue_qk(0, s2);
+          issue_qk(tS0, dQ0, (kbase + (uint32_t)(it.lo0 - it.jlo)) & 1);
           mma_commit(b_sfull(0));
+          if (it.lo0 == it.hi0) mma_commit(b_qempty(0));
         }
-        if (act1) {
-          if (!(ok = mbar_wait(b_pfull(1), it & 1, abort_flag))) break;
-          tc_fence_after();
-          issue_pv(1, s, it > 0);
+        if (ok && it.act1) {
+          if ((ok = mbar_wait(b_qfull(1), qn1 & 1, abort_flag, lim)) && wait_k(it.lo1)) {
+            ++qn1;
+            tc_fence_after();
+            issue_qk(tS1, dQ1, (kbase + (uint32_t)(it.lo1 - it.jlo)) & 1);
+            mma_commit(b_sfull(1));
+            if (it.lo1 == it.hi1) mma_commit(b_qempty(1));
+          }
         }
-        mma_commit(b_kvempty(s));
-        if (more && act1) {
-          issue_qk(1, s2);
-          mma_commit(b_sfull(1));
+        for (int j = it.jlo; ok && j <= it.jhi; ++j) {
+          const uint32_t nk = kbase + (uint32_t)(j - it.jlo), nv = vbase + (uint32_t)(j - it.jlo);
+          // every QK^T reading K(j) has been issued: release its slot when they finish
+          mma_commit(b_kempty(nk & 1));
+          if (!(ok = mbar_wait(b_vfull(nv & 1), (nv >> 1) & 1, abort_flag, lim))) break;
+          const uint32_t knext = (nk + 1) & 1;
+          // tile 0
+          if (j >= it.lo0 && j <= it.hi0) {
+            if (!(ok = mbar_wait(b_pfull(0), pn0 & 1, abort_flag, lim))) break;
+            ++pn0;
+            tc_fence_after();
+            issue_pv(tO0, tS0, nv & 1, j == it.lo0);
+            if (j == it.hi0) {
+              mma_commit(b_ofull(0));
+            } else {
+              if (!wait_k(j + 1)) break;
+              tc_fence_after();
+              issue_qk(tS0, dQ0, knext);
+              mma_commit(b_sfull(0));
+              if (j + 1 == it.hi0) mma_commit(b_qempty(0));  // last use of Q tile 0
+            }
+          }
+          // tile 1
+          if (it.act1 && j >= it.lo1 && j <= it.hi1) {
+            if (!(ok = mbar_wait(b_pfull(1), pn1 & 1, abort_flag, lim))) break;
+            ++pn1;
+            tc_fence_after();
+            issue_pv(tO1, tS1, nv & 1, j == it.lo1);
+            if (j == it.hi1) {
+              mma_commit(b_ofull(1));
+            } else {
+              if (!wait_k(j + 1)) break;
+              tc_fence_after();
+              issue_qk(tS1, dQ1, knext);
+              mma_commit(b_sfull(1));
+              if (j + 1 == it.hi1) mma_commit(b_qempty(1));
+            }
+          }
+          mma_commit(b_vempty(nv & 1));
         }
+        kc = kbase + (uint32_t)(it.jhi - it.jlo + 1);
+        vc = vbase + (uint32_t)(it.jhi - it.jlo + 1);
       }
       if (!ok) raise_error(abort_flag);
-      mma_commit(b_ofull(0));
-      mma_commit(b_ofull(1));
+      mma_drain(b_drain);  // no MMA in flight when TMEM is released
     }
   } else {
     // ------------------------------------------------------------ softmax warps
     const int t = warp >> 2;                 // query tile of this warpgroup
-    const int qt = t ? qt1 : qt0;
     const int row = (warp & 3) * 32 + lane;  // TMEM lane
-    const int i = qt * kBM + row;            // query index
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + (uint32_t)(t * 128);
     const uint32_t tO = tmem + lane_base + (uint32_t)(256 + t * 128);
-    const int tq_lo = qt * kBM, tq_hi = min(tq_lo + kBM - 1, p.Nq - 1);
     const float sl2 = p.scale_log2;
-    float m_used = -INFINITY;  // running row maximum, log2 units (scale included)
-    float l = 0.f;             // running row sum relative to m_used
-    bool ok = (t == 0) || act1;
-    for (int it = 0; ok && it < n_kv; ++it) {
-      const int k0 = (j_lo + it) * kBN;
-      if (!(ok = mbar_wait(b_sfull(t), it & 1, abort_flag))) break;
-      tc_fence_after();
-      uint32_t s[128];
+    uint32_t sn = 0, on = 0;  // S tiles consumed, O tiles consumed
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+      const Item it = decode_item(p, idx);
+      if (t == 1 && !it.act1) continue;
+      const int qt = it.qt0 + t;
+      const int lo_t = t ? it.lo1 : it.lo0, hi_t = t ? it.hi1 : it.hi0;
+      const int i = qt * kBM + row;  // query index
+      const int tq_lo = qt * kBM, tq_hi = min(tq_lo + kBM - 1, p.Nq - 1);
+      // keys this row may see: [key_lo, key_hi]
+      const int key_hi = p.mask == IHA_MASK_NONE ? p.Nk - 1 : min(i, p.Nk - 1);
+      const int key_lo = p.mask == IHA_MASK_CAUSAL_WINDOW ? i - (p.window - 1) : 0;
+      float m_used = -INFINITY;  // running row maximum, log2 units (scale included)
+      float l = 0.f;             // running row sum relative to m_used
+      for (int j = lo_t; j <= hi_t; ++j) {
+        const int k0 = j * kBN;
+        if (!(ok = mbar_wait(b_sfull(t), sn & 1, abort_flag, lim))) break;
+        ++sn;
+        tc_fence_after();
+        const bool full_tile =
+            (k0 + kBN <= p.Nk) &&
+            (p.mask == IHA_MASK_NONE ||
+             (k0 + kBN - 1 <= tq_lo && (p.mask == IHA_MASK_CAUSAL || tq_hi - k0 < p.window)));
+        // visible columns of this tile for this row: [c_lo, c_hi]
+        const int c_lo = max(key_lo - k0, 0), c_hi = min(key_hi - k0, kBN - 1);
+        // pass 1: row maximum (the whole row, four independent max chains)
+        float mt;
+        {
+          uint32_t s[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s + 32 * c);
-      tmem_wait_ld();
-      const bool full_tile =
-          (k0 + kBN <= p.Nk) &&
-          (p.mask == IHA_MASK_NONE ||
-           (k0 + kBN - 1 <= tq_lo &&
-            (p.mask == IHA_MASK_CAUSAL || tq_hi - k0 < p.window)));
-      if (!full_tile) {
-#pragma unroll
-        for (int e = 0; e < 128; ++e) {
-          const int kj = k0 + e;
-          bool vis = kj < p.Nk;
-          if (p.mask != IHA_MASK_NONE) {
-            vis = vis && kj <= i;
-            if (p.mask == IHA_MASK_CAUSAL_WINDOW) vis = vis && (i - kj < p.window);
-          }
-          if (!vis) s[e] = 0xFF800000u;  // -inf
-        }
-      }
-      // row maximum: 8 independent three-input max chains, then a small tree
-      float mx[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) mx[j] = __uint_as_float(s[j]);
-#pragma unroll
-      for (int e = 8; e < 128; e += 16)
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          mx[j] = fmax3f(mx[j], __uint_as_float(s[e + j]), __uint_as_float(s[e + 8 + j]));
-      const float mt = fmaxf(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], fmax3f(mx[5], mx[6], mx[7])));
-      const float m_new = fmaxf(m_used, mt * sl2);
-      bool rescale = false;
-      float factor = 1.f;
-      if (it == 0) {
-        m_used = m_new;
-      } else if (__any_sync(0xffffffffu, m_new > m_used + kRescaleLog2)) {
-        factor = (m_new == -INFINITY) ? 1.f : fast_exp2(m_used - m_new);
-        l *= factor;
-        m_used = m_new;
-        rescale = true;
-      }
-      const float base = (m_used == -INFINITY) ? 0.f : m_used;
-      // P = 2^(s * scale_log2 - base), packed to bf16 pairs over the S columns
-      const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(-base, -base);
-      float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                        make_float2(0.f, 0.f)};
-      uint32_t pk[64];
-#pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        const float2 xx = __ffma2_rn(
-            make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nb2);
-        const float p0 = fast_exp2(xx.x), p1 = fast_exp2(xx.y);
-        sum2[e & 3] = __fadd2_rn(sum2[e & 3], make_float2(p0, p1));
-        pk[e] = pack_bf16x2(p0, p1);
-      }
-      tmem_st32(tS, pk);
-      tmem_st32(tS + 32u, pk + 32);
-      const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
-      const float2 st = __fadd2_rn(s01, s23);
-      l += st.x + st.y;
-      if (rescale) {
-        // O <- O * factor before this tile's P.V is issued (PV of the previous
-        // tile is complete: the S commit waited on above tracks it)
-        uint32_t r[32];
-        for (int c = 0; c < 2 * p.nD; ++c) {
-          tmem_ld32(tO + 32u * c, r);
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s + 32 * c);
           tmem_wait_ld();
+          if (!full_tile) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
-          tmem_st32(tO + 32u * c, r);
+            for (int e = 0; e < 128; ++e)
+              if (e < c_lo || e > c_hi) s[e] = 0xFF800000u;  // -inf
+          }
+          float mx[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) mx[q] = __uint_as_float(s[q]);
+#pragma unroll
+          for (int e = 4; e < 128; e += 8)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              mx[q] = fmax3f(mx[q], __uint_as_float(s[e + q]), __uint_as_float(s[e + 4 + q]));
+          mt = fmaxf(fmax3f(mx[0], mx[1], mx[2]), mx[3]);
         }
+        const float m_new = fmaxf(m_used, mt * sl2);
+        bool rescale = false;
+        float factor = 1.f;
+        if (j == lo_t) {
+          m_used = m_new;
+        } else if (__any_sync(0xffffffffu, m_new > m_used + kRescaleLog2)) {
+          factor = (m_new == -INFINITY) ? 1.f : fast_exp2(m_used - m_new);
+          l *= factor;
+          m_used = m_new;
+          rescale = true;
+        }
+        const float base = (m_used == -INFINITY) ? 0.f : m_used;
+        // pass 2, by halves of 64 columns: P = 2^(s * scale_log2 - base),
+        // packed to bf16 pairs over the S columns (P half h lands in columns
+        // 32h .. 32h+31, below every S column still to be read); pairs 3, 7,
+        // 11, 15 of every 16 use the FMA-pipe polynomial.
+        const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(-base, -base);
+        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t s[64];
+          tmem_ld32(tS + 64u * h, s);
+          tmem_ld32(tS + 64u * h + 32u, s + 32);
+          tmem_wait_ld();
+          if (!full_tile) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (64 * h + e < c_lo || 64 * h + e > c_hi) s[e] = 0xFF800000u;
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float2 xx = __ffma2_rn(
+                make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nb2);
+            float2 pp;
+            if ((e & 3) == 3) {
+              pp = exp2_poly3_x2(xx);
+            } else {
+              pp.x = fast_exp2(xx.x);
+              pp.y = fast_exp2(xx.y);
+            }
+            sum2[e & 1] = __fadd2_rn(sum2[e & 1], pp);
+            pk[e] = pack_bf16x2(pp.x, pp.y);
+          }
+          tmem_st32(tS + 32u * h, pk);
+        }
+        const float2 st = __fadd2_rn(sum2[0], sum2[1]);
+        l += st.x + st.y;
+        if (rescale) {
+          // O <- O * factor before this tile's P.V is issued (P.V of the
+          // previous tile is complete: the S commit waited on above tracks it)
+#pragma unroll
+          for (int c = 0; c < 2 * NCH; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + 32u * c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
+            tmem_st32(tO + 32u * c, r);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(b_pfull(t));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(b_pfull(t));
-    }
-    if ((t == 0) || act1) {
-      if (ok) ok = mbar_wait(b_ofull(t), 0, abort_flag);
-      if (!ok) raise_error(abort_flag);
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = mbar_wait(b_ofull(t), on & 1, abort_flag, lim))) break;
+      ++on;
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.o + bo * p.so_bo + bi * p.so_bi + (int64_t)i * p.so_seq + h * p.so_h;
-      uint32_t r[128];
-      tmem_ld32(tO, r);
-      tmem_ld32(tO + 32u, r + 32);
-      if (p.nD == 2) {
-        tmem_ld32(tO + 64u, r + 64);
-        tmem_ld32(tO + 96u, r + 96);
-      }
-      tmem_wait_ld();
-      if (ok && i < p.Nq) {
+      __nv_bfloat16* orow =
+          p.o + it.bo * p.so_bo + it.bi * p.so_bi + (int64_t)min(i, p.Nq - 1) * p.so_seq +
+          it.h * p.so_h;
 #pragma unroll
-        for (int g8 = 0; g8 < 16; ++g8) {
-          const int f = 8 * g8;
-          if (f < p.d) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[f + 0]) * inv_l, __uint_as_float(r[f + 1]) * inv_l);
-            v.y = pack_bf16x2(__uint_as_float(r[f + 2]) * inv_l, __uint_as_float(r[f + 3]) * inv_l);
-            v.z = pack_bf16x2(__uint_as_float(r[f + 4]) * inv_l, __uint_as_float(r[f + 5]) * inv_l);
-            v.w = pack_bf16x2(__uint_as_float(r[f + 6]) * inv_l, __uint_as_float(r[f + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + f) = v;
+      for (int c = 0; c < NCH; ++c) {  // 64 columns of O at a time
+        uint32_t r[64];
+        tmem_ld32(tO + 64u * c, r);
+        tmem_ld32(tO + 64u * c + 32u, r + 32);
+        tmem_wait_ld();
+        if (i < p.Nq) {
+#pragma unroll
+          for (int g8 = 0; g8 < 8; ++g8) {
+            const int f = 64 * c + 8 * g8;
+            if (f < p.d) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(r[8 * g8 + 0]) * inv_l, __uint_as_float(r[8 * g8 + 1]) * inv_l);
+              v.y = pack_bf16x2(__uint_as_float(r[8 * g8 + 2]) * inv_l, __uint_as_float(r[8 * g8 + 3]) * inv_l);
+              v.z = pack_bf16x2(__uint_as_float(r[8 * g8 + 4]) * inv_l, __uint_as_float(r[8 * g8 + 5]) * inv_l);
+              v.w = pack_bf16x2(__uint_as_float(r[8 * g8 + 6]) * inv_l, __uint_as_float(r[8 * g8 + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(orow + f) = v;
+            }
           }
         }
       }
-      if (ok && p.lse && i < p.Nq) {
+      tc_fence_before();  // O may be overwritten once the next P of this tile is published
+      if (i < p.Nq && p.lse) {
         const float base = (m_used == -INFINITY) ? 0.f : m_used;
-        p.lse[((int64_t)bz * p.Hh + h) * p.Nq + i] =
+        p.lse[((int64_t)it.bz * p.Hh + it.h) * p.Nq + i] =
             l > 0.f ? (base + log2f(l)) * 0.6931471805599453f : -INFINITY;
       }
     }
+    if (!ok) raise_error(abort_flag);
   }
 
   tc_fence_before();
@@ -471,6 +613,22 @@ CUresult make_map(CUtensorMap* m, const void* base, int Bo, int Bi, int N, int H
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+std::once_flag g_tc_attr_once;
+cudaError_t g_tc_attr_err = cudaSuccess;
+
+// Dynamic shared memory attribute of both instantiations, set once per
+// process (thread-safe); the size does not depend on the device.
+cudaError_t set_tc_attributes() {
+  std::call_once(g_tc_attr_once, [] {
+    g_tc_attr_err = cudaFuncSetAttribute(attn_fwd_tc_kernel<1>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (g_tc_attr_err == cudaSuccess)
+      g_tc_attr_err = cudaFuncSetAttribute(attn_fwd_tc_kernel<2>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  return g_tc_attr_err;
+}
+
 iha_status launch_tc(const void* q, const void* k, const void* v, void* o, float* lse, int Bo,
                      int Bi, int Hh, int Nq, int Nk, int d, const iha_strides& sq,
                      const iha_strides& sk, const iha_strides& sv, const iha_strides& so,
@@ -490,7 +648,15 @@ iha_status launch_tc(const void* q, const void* k, const void* v, void* o, float
   p.nD = (d + kChunk - 1) / kChunk;
   p.mask = mask;
   p.window = window;
-  p.n_qpairs = ((Nq + kBM - 1) / kBM + 1) / 2;
+  p.n_qt = (Nq + kBM - 1) / kBM;
+  p.n_qpairs = (p.n_qt + 1) / 2;
+  p.n_hb = Bo * Bi * Hh;
+  const int64_t kv_bytes = 2ll * Nk * d * 2;  // K and V of one head
+  int64_t g = kGroupKVBytes / (kv_bytes > 0 ? kv_bytes : 1);
+  if (g < 1) g = 1;
+  if (g > p.n_hb) g = p.n_hb;
+  p.group = (int)g;
+  p.n_items = p.n_hb * p.n_qpairs;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.so_bo = so.b_outer;
   p.so_bi = so.b_inner;
@@ -498,17 +664,17 @@ iha_status launch_tc(const void* q, const void* k, const void* v, void* o, float
   p.so_h = so.head;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    if (cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return check_launch("mha_fwd (smem attribute)");
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
-  dim3 grid(Hh, Bo * Bi, p.n_qpairs);
-  attn_fwd_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  p.wait_limit_ns = wait_limit_for_next_launch();
+  p.withhold = withhold_for_this_launch() ? 1 : 0;
+  const cudaError_t ae = set_tc_attributes();
+  if (ae != cudaSuccess)
+    return fail(IHA_ERR_CUDA, "mha_fwd (smem attribute): %s", cudaGetErrorString(ae));
+  int grid = sm_count();
+  if (grid > p.n_items) grid = p.n_items;
+  if (p.nD == 1)
+    attn_fwd_tc_kernel<1><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    attn_fwd_tc_kernel<2><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return check_launch("mha_fwd");
 }
 
@@ -533,8 +699,9 @@ extern "C" iha_status mha_fwd(const void* q, const void* k, const void* v, void*
   if (mask_mode != IHA_MASK_NONE && Nq != Nk)
     return fail(IHA_ERR_UNSUPPORTED, "mha_fwd: causal masks need Nq == Nk");
   if (d > 128) return fail(IHA_ERR_UNSUPPORTED, "mha_fwd: d = %d > 128", d);
-  if (Hh > 65535 || (int64_t)B_outer * B_inner > 65535)
-    return fail(IHA_ERR_UNSUPPORTED, "mha_fwd: too many heads or batches for one launch");
+  if ((int64_t)B_outer * B_inner * Hh * (((int64_t)Nq + 255) / 256) > INT32_MAX ||
+      (int64_t)B_outer * B_inner > 65535 || Hh > 65535)
+    return fail(IHA_ERR_UNSUPPORTED, "mha_fwd: too many heads, batches or rows for one launch");
   if (mask_mode != IHA_MASK_CAUSAL_WINDOW) window = 0;
   if (!(scale > 0.f)) scale = 1.f / sqrtf((float)d);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

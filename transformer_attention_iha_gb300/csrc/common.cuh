@@ -12,6 +12,10 @@
 
 namespace iha {
 
+// Every wait in these kernels gives up after this long and reports
+// DEV_ERR_WAIT_TIMEOUT instead of spinning forever.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
 // ---------------------------------------------------------------- host side
 // Records a formatted detail for iha_last_error() and returns `s`.
 iha_status fail(iha_status s, const char* fmt, ...);
@@ -25,6 +29,12 @@ int sm_count();
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
                       void* base, const uint64_t* dims, const uint64_t* strides_bytes,
                       const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+// Wait limit and withheld-load flag for the next kernel launch on this host
+// thread: kWaitLimitNs and false unless iha_test_fail_next_wait() armed a
+// one-shot test of the failure path (consumed by the read).
+uint64_t wait_limit_for_next_launch();
+bool withhold_for_this_launch();
 
 // Device error codes (see iha_device_error in iha.h).
 enum : unsigned { DEV_ERR_KEEP_INDEX = 1u, DEV_ERR_WAIT_TIMEOUT = 2u };
@@ -62,10 +72,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Every wait in these kernels gives up after this long and reports
-// DEV_ERR_WAIT_TIMEOUT instead of spinning forever.
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
-
 // ---- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -93,17 +99,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for phase `parity` of the barrier.  Returns false if the wait
-// gave up (after kWaitLimitNs) or if `abort_flag` (shared) was raised by
-// another thread of the block; the caller then unwinds.
+// gave up (after limit_ns) or if `abort_flag` (shared) was raised by another
+// thread of the block; the caller then unwinds.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// The same wait for a whole warp that goes on to warp-collective tcgen05
+// loads or stores: every lane gets the same answer, so a wait that gives up
+// on one lane while the barrier completes on another cannot split the warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, limit_ns));
 }
 
 // ---- TMA (tiled bulk tensor copies)
@@ -208,6 +224,27 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Issue-only variants for tight MMA loops: no "memory" clobber, so the
+// compiler keeps descriptors in registers across back-to-back issues.  The
+// ordering against shared-memory producers and TMEM consumers comes from the
+// mbarrier waits and tcgen05.commit (volatile asm with memory clobbers)
+// around the loop; volatile asm statements keep their relative order.
+__device__ __forceinline__ void mma_ss_nm(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_ts_nm(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -277,11 +314,29 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       IHA_W32(r)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Waits (bounded) until every tcgen05 operation this thread issued has
+// completed: a commit to the single-use barrier `bar` (count 1, phase 0).
+// Used before tensor memory is released on every exit path.
+__device__ __forceinline__ void mma_drain(uint32_t bar) {
+  mma_commit(bar);
+  volatile int no_abort = 0;
+  mbar_wait(bar, 0, &no_abort);
 }
 
 // ---- misc
@@ -290,6 +345,30 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// 2^x for a pair, on the FMA and integer pipes instead of the MUFU unit.
+// Method: Cody-Waite style range reduction x = j + f with j = round(x) (the
+// 1.5 * 2^23 shifter leaves j in the low mantissa bits) and f in [-1/2, 1/2],
+// then 2^f by a degree-3 polynomial fitted for minimax relative error on
+// [-1/2, 1/2] with the Remez exchange algorithm (max relative error 7.5e-5,
+// far below the 2^-9 of the bf16 probabilities it feeds), and 2^j added
+// into the exponent field.  x is clamped to >= -125 so the exponent stays
+// normal; -inf (masked scores) gives 2^-125 ~ 2e-38 instead of 0.
+__device__ __forceinline__ float2 exp2_poly3_x2(float2 x) {
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  x.x = fmaxf(x.x, -125.f);
+  x.y = fmaxf(x.y, -125.f);
+  const float2 t = __fadd2_rn(x, make_float2(kShift, kShift));
+  const float2 r = __fadd2_rn(t, make_float2(-kShift, -kShift));
+  const float2 f = __fadd2_rn(x, make_float2(-r.x, -r.y));
+  float2 q = __ffma2_rn(make_float2(0.0551716685f, 0.0551716685f), f,
+                        make_float2(0.242611125f, 0.242611125f));
+  q = __ffma2_rn(q, f, make_float2(0.693260968f, 0.693260968f));
+  q = __ffma2_rn(q, f, make_float2(0.999928057f, 0.999928057f));
+  return make_float2(
+      __uint_as_float(__float_as_uint(q.x) + (__float_as_uint(t.x) << 23)),
+      __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
+}
+
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
 __device__ __forceinline__ float fmax3f(float a, float b, float c) {
   float r;

@@ -603,7 +603,7 @@ iha_status iha_premix_bwd_dx(const void* dy, const float* w, void* dx, int B, in
       overlaps(dx, g.ntok * H * d * es, w, (size_t)g.HP * H * 4))
     return fail(IHA_ERR_INVALID_ARG, "iha_premix_bwd_dx: dx overlaps an input");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (dt == IHA_BF16 && premix_bwd_tc_supported(H, P, d))
+  if (dt == IHA_BF16 && premix_bwd_tc_supported(H, P, d, true, false, rope != 0))
     return premix_bwd_tc(dy, nullptr, w, dx, nullptr, B, N, H, P, d, rope, rope_base, s);
   if (dt == IHA_BF16) launch_dx<__nv_bfloat16>(g, dy, w, dx, rope != 0, s);
   else launch_dx<float>(g, dy, w, dx, rope != 0, s);
@@ -624,7 +624,7 @@ iha_status iha_premix_bwd_dw(const void* dy, const void* x, float* dw, int B, in
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dt == IHA_BF16) {
     zero_f32_kernel<<<1, 256, 0, s>>>(dw, g.HP * H);
-    if (premix_bwd_tc_supported(H, P, d))
+    if (premix_bwd_tc_supported(H, P, d, false, true, rope != 0))
       return premix_bwd_tc(dy, x, nullptr, nullptr, dw, B, N, H, P, d, rope, rope_base, s);
     st = launch_dw_mma(g, dy, x, dw, rope != 0, s);
     if (st != IHA_OK) return st;
@@ -655,7 +655,7 @@ iha_status iha_premix_bwd(const void* dy, const void* x, const float* w, void* d
       overlaps(dw, nw, dx, nx))
     return fail(IHA_ERR_INVALID_ARG, "iha_premix_bwd: an output overlaps another buffer");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (dt == IHA_BF16 && premix_bwd_tc_supported(H, P, d)) {
+  if (dt == IHA_BF16 && premix_bwd_tc_supported(H, P, d, true, true, rope != 0)) {
     zero_f32_kernel<<<1, 256, 0, s>>>(dw, g.HP * H);
     return premix_bwd_tc(dy, x, w, dx, dw, B, N, H, P, d, rope, rope_base, s);
   }

@@ -86,7 +86,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto b_xempty = [&](int s) { return bar0 + 8u * (kXStages + s); };
   auto b_accfull = [&](int a) { return bar0 + 8u * (2 * kXStages + a); };
   auto b_accempty = [&](int a) { return bar0 + 8u * (2 * kXStages + 2 + a); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kXStages + 4);
+  const uint32_t b_drain = bar0 + 8u * (2 * kXStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kXStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_accfull(a), 1);
       mbar_init(b_accempty(a), kEpiThreads);
     }
+    mbar_init(b_drain, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -149,12 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(b_xfull(xs), p.stage_bytes);
         tma_load_4d(sX + xs * p.stage_bytes, &tmX, b_xfull(xs), 0, 0, 0, g * kTok);
       }
-      if (*abort_flag) {
-        // let the copies still in flight land before the CTA exits
-        volatile int no_abort = 0;
-        for (int kk = k - kXStages > 0 ? k - kXStages : 0; kk < k; ++kk)
-          mbar_wait(b_xfull(kk % kXStages), (kk / kXStages) & 1, &no_abort);
-      }
+      // Whoever aborted, no copy may still be landing when the CTA exits
+      // (in a normal run the last loads have completed and this returns at once).
+      volatile int no_abort = 0;
+      for (int kk = k - kXStages > 0 ? k - kXStages : 0; kk < k; ++kk)
+        mbar_wait(b_xfull(kk % kXStages), (kk / kXStages) & 1, &no_abort);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(b_accfull(a));
       }
       if (!ok) raise_error(abort_flag);
+      mma_drain(b_drain);  // no MMA in flight when TMEM is released
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -203,10 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (!mbar_wait(b_accfull(a), (k >> 1) & 1, abort_flag)) raise_error(abort_flag);
+      // after an abort: no TMEM loads and no stores, only the arrivals
+      const bool live = mbar_wait_warp(b_accfull(a), (k >> 1) & 1, abort_flag);
+      if (!live) raise_error(abort_flag);
       tc_fence_after();
       float v[D];
-      if (warp_active) {
+      if (warp_active && live) {
         const uint32_t col = tmem + lane_base + (uint32_t)(a * 256 + tt * D);
 #pragma unroll
         for (int c = 0; c < 2 * NCH; ++c) tmem_ld32(col + 32u * c, reinterpret_cast<uint32_t*>(v) + 32 * c);
@@ -214,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(b_accempty(a));
+      if (!live) break;
       if (warp_active && t < p.ntok) {
         if (lane == 0) bulk_wait_read<1>();  // this warp's buffer sb is free again
         __syncwarp();
@@ -365,7 +370,13 @@ namespace iha {
 namespace {
 
 constexpr int kBwdThreads = 384;
-constexpr int kBwdNA = 7;  // dX accumulator slots of 64 TMEM columns
+constexpr int kBwdNA = 6;  // dX accumulator slots of 64 TMEM columns
+// dW partials: the tensor core accumulates at most this many tokens (d/16
+// MMA K-steps each) into one of two 64-column TMEM buffers; the partial is
+// then added into fp32 registers with round-to-nearest adds.  Long chains of
+// tensor-core accumulation drift systematically (measured 3e-5 relative at
+// 216 tokens per CTA); chunks of 8 tokens keep it near fp32 rounding.
+constexpr int kDwChunk = 8;
 
 struct BwdParams {
   int ntok, N, H, HP, hp_pad, nkb, ns;
@@ -415,8 +426,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto b_accempty = [&](int a) { return bar0 + 8u * (2 * NS + 8 + a); };
   auto b_xrfull = [&](int s) { return bar0 + 8u * (2 * NS + 16 + s); };
   auto b_xrempty = [&](int s) { return bar0 + 8u * (2 * NS + 18 + s); };
-  const uint32_t b_dwfull = bar0 + 8u * (2 * NS + 20);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NS + 21);
+  auto b_dwfull = [&](int b) { return bar0 + 8u * (2 * NS + 20 + b); };
+  auto b_dwempty = [&](int b) { return bar0 + 8u * (2 * NS + 22 + b); };
+  const uint32_t b_drain = bar0 + 8u * (2 * NS + 24);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NS + 25);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -435,7 +448,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(b_xrfull(s), 64);
       mbar_init(b_xrempty(s), 1);
     }
-    mbar_init(b_dwfull, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(b_dwfull(b), 1);
+      mbar_init(b_dwempty(b), 128);
+    }
+    mbar_init(b_drain, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -482,7 +499,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_dw = tmem + (uint32_t)(kBwdNA * 64);
+  const uint32_t tmem_dw = tmem + (uint32_t)(kBwdNA * 64);  // + 64 * buffer
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -505,11 +522,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(st + p.dy_bytes + 4096u, &tmX, b_infull(s), 64, 0, tok);
         }
       }
-      if (*abort_flag) {
-        volatile int no_abort = 0;
-        for (int kk = k - NS > 0 ? k - NS : 0; kk < k; ++kk)
-          mbar_wait(b_infull(kk % NS), (kk / NS) & 1, &no_abort);
-      }
+      // Whoever aborted, no copy may still be landing when the CTA exits.
+      volatile int no_abort = 0;
+      for (int kk = k - NS > 0 ? k - NS : 0; kk < k; ++kk)
+        mbar_wait(b_infull(kk % NS), (kk / NS) & 1, &no_abort);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -535,6 +551,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_commit(b_accfull(a));
         }
         if (DO_DW) {
+          const int dwc = k / kDwChunk, dwb = dwc & 1;
+          const bool dw_first = (k % kDwChunk) == 0;
+          if (dw_first && dwc >= 2 &&
+              !(ok = mbar_wait(b_dwempty(dwb), ((dwc >> 1) - 1) & 1, abort_flag))) break;
           uint32_t xsrc = st + p.dy_bytes;
           uint32_t xchunk = 4096u;
           if (PREP) {
@@ -546,16 +566,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t aoff = (uint32_t)(kk >> 2) * p.chunk + (uint32_t)(kk & 3) * 32u;
             const uint32_t boff = (uint32_t)(kk >> 2) * xchunk + (uint32_t)(kk & 3) * 32u;
-            mma_ss(tmem_dw, smem_desc_sw128(st + aoff, 16, 1024),
+            mma_ss(tmem_dw + (uint32_t)(64 * dwb), smem_desc_sw128(st + aoff, 16, 1024),
                    smem_desc_sw128(xsrc + boff, 16, 1024), idesc_dw,
-                   (k > 0 || kk > 0) ? 1u : 0u);
+                   (!dw_first || kk > 0) ? 1u : 0u);
           }
           if (PREP) mma_commit(b_xrempty(k & 1));
+          if ((k % kDwChunk) == kDwChunk - 1 || k == n_my - 1) mma_commit(b_dwfull(dwb));
         }
         mma_commit(b_inempty(s));
       }
       if (!ok) raise_error(abort_flag);
-      mma_commit(b_dwfull);
+      mma_drain(b_drain);  // no MMA in flight when TMEM is released
     }
   } else if (warp >= 10) {
     // ------------------------------------------------------------ R X (hi / lo)
@@ -613,28 +634,69 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------------------ dX epilogue
     // Warp e: features f = 32*(e%4) + lane of the tokens k with k % 2 == e / 4.
+    // Warps 0-3 also fold each dW chunk (TMEM lanes = pseudo-head rows f) into
+    // fp32 registers and add them to dw at the end.
     const int G = warp >> 2, q = warp & 3;
     const int f = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const uint32_t wout = sOut + (uint32_t)(warp * 2) * p.out_bytes;
+    float dwacc[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) dwacc[e] = 0.f;
+    bool ok = true;
+    // fold dW chunk c (all its tokens' MMAs are committed to dwfull(c & 1))
+    auto fold_dw = [&](int c) {
+      const int b = c & 1;
+      if (!(ok = mbar_wait_warp(b_dwfull(b), (c >> 1) & 1, abort_flag))) return;
+      tc_fence_after();
+      uint32_t r[32];
+      tmem_ld32(tmem_dw + lane_base + (uint32_t)(64 * b), r);
+      if (PREP) {
+        uint32_t r2[32];
+        tmem_ld32(tmem_dw + lane_base + (uint32_t)(64 * b + 32), r2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dwacc[e] += __uint_as_float(r[e]) + __uint_as_float(r2[e]);
+      } else {
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dwacc[e] += __uint_as_float(r[e]);
+      }
+      tc_fence_before();
+      mbar_arrive(b_dwempty(b));
+    };
+    const int n_dwc = (n_my + kDwChunk - 1) / kDwChunk;
+    int dwc_done = 0;
     int it = 0;
     if (DO_DX) {
+      // After an abort the loop keeps stepping (TMEM and stores skipped) so
+      // that the two warps of an inverse-RoPE pair still meet at every named
+      // barrier; every later wait returns at once on the raised flag.
       for (int k = G; k < n_my; k += 2, ++it) {
         const int tok = blockIdx.x + k * gridDim.x;
         const int a = k % kBwdNA;
         float c = 1.f, sn = 0.f;
         if (ROPE) rope_cos_sin(tok % p.N, p.rt.hi[f & 63], p.rt.lo[f & 63], c, sn);
-        if (!mbar_wait(b_accfull(a), (k / kBwdNA) & 1, abort_flag)) raise_error(abort_flag);
-        tc_fence_after();
-        uint32_t r[32], r2[32];
-        tmem_ld32(tmem + lane_base + (uint32_t)(a * 64), r);
-        tmem_ld32(tmem + lane_base + (uint32_t)(a * 64 + 32), r2);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(b_accempty(a));
+        const bool live = ok && mbar_wait_warp(b_accfull(a), (k / kBwdNA) & 1, abort_flag);
+        if (ok && !live) {
+          ok = false;
+          raise_error(abort_flag);
+        }
         float v[32];
+        if (live) {
+          tc_fence_after();
+          uint32_t r[32], r2[32];
+          tmem_ld32(tmem + lane_base + (uint32_t)(a * 64), r);
+          tmem_ld32(tmem + lane_base + (uint32_t)(a * 64 + 32), r2);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(b_accempty(a));
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) + __uint_as_float(r2[e]);
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) + __uint_as_float(r2[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+        }
         if (EXCH) {
           // inverse rotation: swap with the warp holding features f ^ 64
           float* mine = reinterpret_cast<float*>(gen(sEx + (uint32_t)(warp * 2 + (it & 1)) * p.ex_bytes));
@@ -649,6 +711,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (e < p.H) v[e] = fmaf(v[e], c, theirs[e * 32 + lane] * sg);
         }
+        if (!live) continue;
         if (lane == 0) bulk_wait_read<1>();  // buffer it & 1 is free again
         __syncwarp();
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(gen(wout + (uint32_t)(it & 1) * p.out_bytes));
@@ -661,29 +724,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_store_3d(&tmDX, wout + (uint32_t)(it & 1) * p.out_bytes, q * 32, 0, tok);
           bulk_commit();
         }
+        // a dW chunk is complete once the last even token of it has passed
+        if (DO_DW && G == 0 && (k + 2 >= n_my || (k + 2) / kDwChunk != k / kDwChunk)) {
+          fold_dw(dwc_done);
+          ++dwc_done;
+          if (!ok) raise_error(abort_flag);
+        }
       }
       if (lane == 0) bulk_wait<0>();
     }
     if (DO_DW && G == 0) {
-      if (!mbar_wait(b_dwfull, 0, abort_flag)) raise_error(abort_flag);
-      tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32(tmem_dw + lane_base, r);
-      if (PREP) {
-        uint32_t r2[32];
-        tmem_ld32(tmem_dw + lane_base + 32u, r2);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
-      } else {
-        tmem_wait_ld();
-      }
-      if (f < p.HP && n_my > 0) {
+      for (; ok && dwc_done < n_dwc; ++dwc_done) fold_dw(dwc_done);
+      if (ok && f < p.HP && n_my > 0) {
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          if (e < p.H) atomicAdd(dw + f * p.H + e, __uint_as_float(r[e]));
+          if (e < p.H) atomicAdd(dw + f * p.H + e, dwacc[e]);
       }
     }
+    if (!ok) raise_error(abort_flag);
   }
 
   tc_fence_before();
@@ -696,35 +754,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 }  // namespace
 
-bool premix_bwd_tc_supported(int H, int P, int d) { return d == 128 && H <= 32 && H * P <= 128; }
+namespace {
+
+// Launch geometry of the backward kernel; returns false when even the
+// two-stage ring does not fit in shared memory.
+bool bwd_geometry(int H, int P, bool do_dx, bool do_dw, bool rope, BwdParams* p, size_t* smem) {
+  const bool exch = rope && do_dx, prep = rope && do_dw;
+  p->H = H;
+  p->HP = H * P;
+  p->hp_pad = (p->HP + 15) / 16 * 16;
+  p->nkb = (p->hp_pad + 63) / 64;
+  p->chunk = (uint32_t)p->hp_pad * 128u;
+  p->dy_bytes = 2u * p->chunk;
+  p->x_bytes = do_dw ? 2u * 32u * 128u : 0u;
+  // The dW MMA reads each 64-feature dY box as an M = 128 row operand
+  // (16 KB from the box start) whatever hp_pad is; rows >= H*P only feed
+  // discarded accumulator rows, but the bytes must lie inside the stage.
+  uint32_t need = p->dy_bytes + p->x_bytes;
+  if (do_dw && need < p->chunk + 16384u) need = p->chunk + 16384u;
+  p->stage_bytes = (need + 1023u) / 1024u * 1024u;
+  p->out_bytes = ((uint32_t)H * 64u + 127u) / 128u * 128u;
+  p->ex_bytes = ((uint32_t)H * 128u + 127u) / 128u * 128u;
+  const size_t fixed = 1024 + (do_dx ? (size_t)p->nkb * 8192u : 0) + (prep ? 32768 : 0) +
+                       (do_dx ? 16u * p->out_bytes : 0) + (exch ? 16u * p->ex_bytes : 0) +
+                       (prep ? 512 : 0) + 512;  // last: barriers (<= 2*4 + 25 slots)
+  const size_t limit = 227 * 1024;
+  p->ns = 4;
+  while (p->ns > 2 && fixed + (size_t)p->ns * p->stage_bytes > limit) --p->ns;
+  *smem = fixed + (size_t)p->ns * p->stage_bytes;
+  return *smem <= limit;
+}
+
+}  // namespace
+
+bool premix_bwd_tc_supported(int H, int P, int d, bool do_dx, bool do_dw, bool rope) {
+  if (d != 128 || H > 32 || H * P > 128) return false;
+  BwdParams p;
+  size_t smem;
+  return bwd_geometry(H, P, do_dx, do_dw, rope, &p, &smem);
+}
 
 iha_status premix_bwd_tc(const void* dy, const void* x, const float* w, void* dx, float* dw,
                          int B, int N, int H, int P, int d, int rope, float rope_base,
                          cudaStream_t stream) {
   const bool do_dx = dx != nullptr, do_dw = dw != nullptr;
-  const bool exch = rope && do_dx, prep = rope && do_dw;
   BwdParams p;
+  size_t smem;
+  if (!bwd_geometry(H, P, do_dx, do_dw, rope != 0, &p, &smem))
+    return fail(IHA_ERR_UNSUPPORTED, "premix backward: shared memory budget");
   p.ntok = B * N;
   p.N = N;
-  p.H = H;
-  p.HP = H * P;
-  p.hp_pad = (p.HP + 15) / 16 * 16;
-  p.nkb = (p.hp_pad + 63) / 64;
-  p.chunk = (uint32_t)p.hp_pad * 128u;
-  p.dy_bytes = 2u * p.chunk;
-  p.x_bytes = do_dw ? 2u * 32u * 128u : 0u;
-  p.stage_bytes = (p.dy_bytes + p.x_bytes + 1023u) / 1024u * 1024u;
-  p.out_bytes = ((uint32_t)H * 64u + 127u) / 128u * 128u;
-  p.ex_bytes = ((uint32_t)H * 128u + 127u) / 128u * 128u;
   make_rope_table(&p.rt, d, rope_base);
-  const size_t fixed = 1024 + (do_dx ? (size_t)p.nkb * 8192u : 0) + (prep ? 32768 : 0) +
-                       (do_dx ? 16u * p.out_bytes : 0) + (exch ? 16u * p.ex_bytes : 0) +
-                       (prep ? 512 : 0) + 512;
-  const size_t limit = 227 * 1024;
-  p.ns = 4;
-  while (p.ns > 2 && fixed + (size_t)p.ns * p.stage_bytes > limit) --p.ns;
-  const size_t smem = fixed + (size_t)p.ns * p.stage_bytes;
-  if (smem > limit) return fail(IHA_ERR_UNSUPPORTED, "premix backward: shared memory budget");
 
   CUtensorMap mdy, mx, mdx;
   {

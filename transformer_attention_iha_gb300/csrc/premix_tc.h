@@ -20,8 +20,9 @@ void make_rope_table(RopeTable* rt, int d, float base);
 // H*P <= 128.
 bool premix_tc_supported(int H, int P, int d);
 
-// Backward shapes: bf16, d = 128, H <= 32, H*P <= 128.
-bool premix_bwd_tc_supported(int H, int P, int d);
+// Backward shapes: bf16, d = 128, H <= 32, H*P <= 128, and the kernel variant
+// (dX and / or dW, with or without RoPE) fits in shared memory.
+bool premix_bwd_tc_supported(int H, int P, int d, bool do_dx, bool do_dw, bool rope);
 
 // dX (if dx != nullptr) and dW (if dw != nullptr, accumulated with atomics
 // into a zeroed dw) in one pass over dY.
