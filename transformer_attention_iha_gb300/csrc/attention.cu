@@ -46,7 +46,8 @@ constexpr int kBN = 128;             // keys per tile
 constexpr int kChunk = 64;           // head-dim elements per 128-byte swizzle row
 constexpr int kTileChunkBytes = kBM * 128;  // 16 KB: 128 rows x 64 bf16
 constexpr int kThreads = 320;
-constexpr int kSmemTiles = 12 * kTileChunkBytes;  // Q 2x2, K 2x2, V 2x2 chunks
+constexpr int kKSlots = 3;           // K ring depth (V ring: 2)
+constexpr int kSmemTiles = (4 + 2 * kKSlots + 4) * kTileChunkBytes;  // Q 2x2, K 3x2, V 2x2 chunks
 constexpr int kSmemBytes = kSmemTiles + 256 + 1024;  // + barriers + alignment slack
 constexpr float kRescaleLog2 = 8.0f;
 // L2 budget for the K / V of one head group.
@@ -132,21 +133,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sQ = smem_u32(smem);                       // [tile][chunk]
-  const uint32_t sK = sQ + 4 * kTileChunkBytes;             // [slot][chunk]
-  const uint32_t sV = sK + 4 * kTileChunkBytes;             // [slot][chunk]
+  const uint32_t sK = sQ + 4 * kTileChunkBytes;             // [slot][chunk], 3 slots
+  const uint32_t sV = sK + 2 * kKSlots * kTileChunkBytes;   // [slot][chunk], 2 slots
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemTiles);
   const uint32_t bar0 = smem_u32(bars);
   auto b_qfull = [&](int t) { return bar0 + 8u * (0 + t); };
   auto b_qempty = [&](int t) { return bar0 + 8u * (2 + t); };
-  auto b_kfull = [&](int s) { return bar0 + 8u * (4 + s); };
-  auto b_kempty = [&](int s) { return bar0 + 8u * (6 + s); };
-  auto b_vfull = [&](int s) { return bar0 + 8u * (8 + s); };
-  auto b_vempty = [&](int s) { return bar0 + 8u * (10 + s); };
-  auto b_sfull = [&](int t) { return bar0 + 8u * (12 + t); };
-  auto b_pfull = [&](int t) { return bar0 + 8u * (14 + t); };
-  auto b_ofull = [&](int t) { return bar0 + 8u * (16 + t); };
-  const uint32_t b_drain = bar0 + 8u * 18;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  auto b_kfull = [&](int s) { return bar0 + 8u * (4 + s); };    // 3 slots
+  auto b_kempty = [&](int s) { return bar0 + 8u * (7 + s); };   // 3 slots
+  auto b_vfull = [&](int s) { return bar0 + 8u * (10 + s); };
+  auto b_vempty = [&](int s) { return bar0 + 8u * (12 + s); };
+  auto b_sfull = [&](int t) { return bar0 + 8u * (14 + t); };
+  auto b_pfull = [&](int t) { return bar0 + 8u * (16 + t); };
+  auto b_ofull = [&](int t) { return bar0 + 8u * (18 + t); };
+  const uint32_t b_drain = bar0 + 8u * 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -154,11 +155,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kChunkBytes = (uint32_t)NCH * kTileChunkBytes;
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < kKSlots; ++s) {
+      mbar_init(b_kfull(s), 1);
+      mbar_init(b_kempty(s), 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(b_qfull(s), 1);
       mbar_init(b_qempty(s), 1);
-      mbar_init(b_kfull(s), 1);
-      mbar_init(b_kempty(s), 1);
       mbar_init(b_vfull(s), 1);
       mbar_init(b_vempty(s), 1);
       mbar_init(b_sfull(s), 1);
@@ -198,11 +201,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // load number n of the K (is_v = false) or V ring; returns the new count
       auto load_kv = [&](const Item& it, int j, bool is_v, uint32_t n) -> uint32_t {
-        const int s = n & 1;
+        const uint32_t depth = is_v ? 2u : (uint32_t)kKSlots;
+        const int s = (int)(n % depth);
         if (is_v && n == 0 && p.withhold && blockIdx.x == 0)
           return n + 1;  // withheld: its consumer's wait runs out (failure-path test)
-        if (n >= 2 && !(ok = mbar_wait(is_v ? b_vempty(s) : b_kempty(s), ((n >> 1) - 1) & 1,
-                                       abort_flag, lim)))
+        if (n >= depth && !(ok = mbar_wait(is_v ? b_vempty(s) : b_kempty(s),
+                                           ((n / depth) - 1) & 1, abort_flag, lim)))
           return n;
         const uint32_t full = is_v ? b_vfull(s) : b_kfull(s);
         mbar_arrive_expect_tx(full, kChunkBytes);
@@ -227,12 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // for the last load issued into every slot (in a normal run each has
       // completed already and the wait returns at once).
       volatile int no_abort = 0;
-      for (int s = 0; s < 2; ++s) {
-        if (kc > (uint32_t)s)
-          mbar_wait(b_kfull(s), ((kc - 1 - ((kc - 1 - s) & 1)) >> 1) & 1, &no_abort, lim);
-        if (vc > (uint32_t)s)
-          mbar_wait(b_vfull(s), ((vc - 1 - ((vc - 1 - s) & 1)) >> 1) & 1, &no_abort, lim);
-      }
+      for (uint32_t n = kc > (uint32_t)kKSlots ? kc - kKSlots : 0; n < kc; ++n)
+        mbar_wait(b_kfull(n % kKSlots), (n / kKSlots) & 1, &no_abort, lim);
+      for (uint32_t n = vc > 2u ? vc - 2u : 0; n < vc; ++n)
+        mbar_wait(b_vfull(n & 1), (n >> 1) & 1, &no_abort, lim);
       if (qn0 > 0) mbar_wait(b_qfull(0), (qn0 - 1) & 1, &no_abort, lim);
       if (qn1 > 0) mbar_wait(b_qfull(1), (qn1 - 1) & 1, &no_abort, lim);
     }
@@ -248,13 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQ0 = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t dQ1 = smem_desc_sw128(sQ + 2 * kTileChunkBytes, 16, 1024);
       const uint64_t dK0 = smem_desc_sw128(sK, 16, 1024);
-      const uint64_t dK1 = smem_desc_sw128(sK + 2 * kTileChunkBytes, 16, 1024);
+      constexpr uint64_t kKSlotDesc = (uint64_t)((2 * kTileChunkBytes) >> 4);  // one K slot
       const uint64_t dV0 = smem_desc_sw128(sV, kTileChunkBytes, 1024);
       const uint64_t dV1 = smem_desc_sw128(sV + 2 * kTileChunkBytes, kTileChunkBytes, 1024);
       uint32_t kc = 0, vc = 0, qn0 = 0, qn1 = 0, pn0 = 0, pn1 = 0;
       bool ok = true;
       auto issue_qk = [&](uint32_t dS, uint64_t dq, uint32_t kslot) {
-        const uint64_t dk = kslot ? dK1 : dK0;
+        const uint64_t dk = dK0 + kKSlotDesc * kslot;
 #pragma unroll
         for (int kk = 0; kk < 4 * NCH; ++kk) {
           const uint64_t off = (uint64_t)(((kk >> 2) * kTileChunkBytes + (kk & 3) * 32) >> 4);
@@ -276,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t q = (uint32_t)(j - it.jlo);
           while (ok && k_ready <= q) {
             const uint32_t n = kbase + k_ready;
-            ok = mbar_wait(b_kfull(n & 1), (n >> 1) & 1, abort_flag, lim);
+            ok = mbar_wait(b_kfull(n % kKSlots), (n / kKSlots) & 1, abort_flag, lim);
             ++k_ready;
           }
           return ok;
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((ok = mbar_wait(b_qfull(0), qn0 & 1, abort_flag, lim)) && wait_k(it.lo0)) {
           ++qn0;
           tc_fence_after();
-          issue_qk(tS0, dQ0, (kbase + (uint32_t)(it.lo0 - it.jlo)) & 1);
+          issue_qk(tS0, dQ0, (kbase + (uint32_t)(it.lo0 - it.jlo)) % kKSlots);
           mma_commit(b_sfull(0));
           if (it.lo0 == it.hi0) mma_commit(b_qempty(0));
         }
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((ok = mbar_wait(b_qfull(1), qn1 & 1, abort_flag, lim)) && wait_k(it.lo1)) {
             ++qn1;
             tc_fence_after();
-            issue_qk(tS1, dQ1, (kbase + (uint32_t)(it.lo1 - it.jlo)) & 1);
+            issue_qk(tS1, dQ1, (kbase + (uint32_t)(it.lo1 - it.jlo)) % kKSlots);
             mma_commit(b_sfull(1));
             if (it.lo1 == it.hi1) mma_commit(b_qempty(1));
           }
@@ -301,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = it.jlo; ok && j <= it.jhi; ++j) {
           const uint32_t nk = kbase + (uint32_t)(j - it.jlo), nv = vbase + (uint32_t)(j - it.jlo);
           // every QK^T reading K(j) has been issued: release its slot when they finish
-          mma_commit(b_kempty(nk & 1));
+          mma_commit(b_kempty(nk % kKSlots));
           if (!(ok = mbar_wait(b_vfull(nv & 1), (nv >> 1) & 1, abort_flag, lim))) break;
-          const uint32_t knext = (nk + 1) & 1;
+          const uint32_t knext = (nk + 1) % kKSlots;
           // tile 0
           if (j >= it.lo0 && j <= it.hi0) {
             if (!(ok = mbar_wait(b_pfull(0), pn0 & 1, abort_flag, lim))) break;
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!full_tile) {
 #pragma unroll
             for (int e = 0; e < 128; ++e)
-              if (e < c_lo || e > c_hi) s[e] = 0xFF800000u;  // -inf
+              s[e] = sel_u32(e < c_lo || e > c_hi, 0xFF800000u, s[e]);  // -inf outside
           }
           float mx[4];
 #pragma unroll
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!full_tile) {
 #pragma unroll
             for (int e = 0; e < 64; ++e)
-              if (64 * h + e < c_lo || 64 * h + e > c_hi) s[e] = 0xFF800000u;
+              s[e] = sel_u32(64 * h + e < c_lo || 64 * h + e > c_hi, 0xFF800000u, s[e]);
           }
           uint32_t pk[32];
 #pragma unroll

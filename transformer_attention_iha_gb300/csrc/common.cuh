@@ -369,6 +369,16 @@ __device__ __forceinline__ float2 exp2_poly3_x2(float2 x) {
       __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
 }
 
+// c ? a : b without a branch (one selp; a per-lane condition on a register
+// array element must not become a divergent branch per element).
+__device__ __forceinline__ uint32_t sel_u32(bool c, uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\tselp.b32 %0, %2, %3, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)c), "r"(a), "r"(b));
+  return r;
+}
+
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
 __device__ __forceinline__ float fmax3f(float a, float b, float c) {
   float r;
