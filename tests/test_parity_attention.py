@@ -92,6 +92,30 @@ def test_attention_bf16_many_items_per_cta(T, case):
     assert T.device_error() == 0
 
 
+# Short sequences (Nq == Nk <= 64, no mask) take the packed kernel: two
+# sequences per 128-row tile.  Edges: fewer than 64 tokens, d not a multiple
+# of 16, an odd number of sequences (the last tile has one), several heads.
+SHORT_CASES = [  # (Bo, Bi, T, Hh, d)
+    (3, 1, 49, 2, 96),
+    (1, 7, 64, 1, 128),
+    (5, 1, 1, 3, 64),
+    (2, 3, 33, 1, 40),
+    (1, 1, 64, 1, 96),
+    (4, 2, 64, 3, 16),
+]
+
+
+@pytest.mark.parametrize("case", SHORT_CASES)
+def test_attention_bf16_short_sequences_packed(T, case):
+    Bo, Bi, Tn, Hh, d = case
+    q, k, v = _qkv((Bo, Bi, Tn, Hh, d), (Bo, Bi, Tn, Hh, d), seed=Tn + d + Hh)
+    o, lse = T.mha_fwd(to_dev(q), to_dev(k), to_dev(v), return_lse=True)
+    ro, rl = O.attention(q, k, v)
+    assert_bf16_close(to_f64(o), ro, f"O {case}")
+    _lse_close(to_f64(lse), rl, f"lse {case}")
+    assert T.device_error() == 0
+
+
 def test_attention_bf16_nq_ne_nk(T):
     q, _, _ = _qkv((2, 200, 3, 128), (2, 333, 3, 128), seed=7)
     _, k, v = _qkv((2, 333, 3, 128), (2, 333, 3, 128), seed=8)

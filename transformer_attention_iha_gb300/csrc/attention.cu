@@ -35,6 +35,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "mu_attention.h"
 
 namespace iha {
 namespace {
@@ -715,6 +716,9 @@ extern "C" iha_status mha_fwd(const void* q, const void* k, const void* v, void*
       return fail(IHA_ERR_ALIGNMENT, "mha_fwd: strides must be multiples of 8 elements");
     if (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3))
       return fail(IHA_ERR_ALIGNMENT, "mha_fwd: lse_out must be 4-byte aligned");
+    if (mu_attention_supported(Nq, Nk, d, mask_mode))
+      return mu_attention_fwd(q, k, v, o, lse_out, B_outer, B_inner, Hh, Nq, d, sq, sk, sv, so,
+                              scale, s);
     return launch_tc(q, k, v, o, lse_out, B_outer, B_inner, Hh, Nq, Nk, d, sq, sk, sv, so, scale,
                      mask_mode, window, s);
   }

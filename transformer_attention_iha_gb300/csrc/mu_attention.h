@@ -1,0 +1,20 @@
+// Internal interface of the short-sequence (mask-unit) attention kernel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "iha.h"
+
+namespace iha {
+
+// Sequences the packed kernel handles: no mask, Nq == Nk <= 64, d <= 128.
+bool mu_attention_supported(int Nq, int Nk, int d, int mask);
+
+// Softmax attention of every (b_outer, b_inner, head) sequence of T tokens,
+// two sequences per 128-row tile; arguments as mha_fwd (bf16, validated).
+iha_status mu_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int Bo, int Bi, int Hh, int T, int d, const iha_strides& sq,
+                            const iha_strides& sk, const iha_strides& sv, const iha_strides& so,
+                            float scale, cudaStream_t stream);
+
+}  // namespace iha
