@@ -10,7 +10,9 @@ bf16 inputs (uint16 bit patterns) are widened to float32 exactly before the
 call; results come back as float64.
 
 Sources: "IHA-CUDA: Interleaved Head Attention Kernels for Hopper GPUs",
-sections "Pseudo-Token Mixing (Triton Premix Kernels)" and "FLOP Matching";
+sections "Pseudo-Token Mixing (Triton Premix Kernels)" and "FLOP Matching",
+and "Repository Structure" / "End-to-End Training Benchmark" (the attention
+backward of the training step);
 "hiera-optim 0.1.0", README item 2 (gather / scatter) and
 hiera_optim/attention/mask_unit.py (MaskUnitAttentionFast.forward).
 Every oracle function is pinned by a CPU test against values the pages or the
@@ -46,6 +48,7 @@ def lib() -> C.CDLL:
                                        lp, lp, lp, d, i, l]
         L.oracle_attention_rows.argtypes = [fp, fp, fp, lp, l, dp, dp, l, l,
                                             lp, lp, lp, d, i, l]
+        L.oracle_attention_bwd.argtypes = [fp, fp, fp, fp, dp, dp, dp, l, l, l, l, d, i, l]
         L.oracle_tile_visits.argtypes = [l, l, i, l, l, l]
         L.oracle_tile_visits.restype = l
         for name in ("oracle_mu_gather", "oracle_mu_scatter"):
@@ -174,6 +177,25 @@ def attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: np.ndarray
                                 Nk, d, _p(sq, C.c_long), _p(sk, C.c_long), _p(sv, C.c_long),
                                 float(scale), int(mask), int(window))
     return o, lse
+
+
+def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,
+                  mask: int = 0, window: int = 0, scale: float | None = None):
+    """Gradients (dQ, dK, dV) of attention over dense [B, N, Hh, d] tensors
+    (float32 or bf16 bits) for the upstream gradient dout; float64 results."""
+    qf, kf, vf, gf = _as_f32(q), _as_f32(k), _as_f32(v), _as_f32(dout)
+    B, N, Hh, d = qf.shape
+    assert kf.shape == vf.shape == gf.shape == qf.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = np.empty(qf.shape, dtype=np.float64)
+    dk = np.empty(qf.shape, dtype=np.float64)
+    dv = np.empty(qf.shape, dtype=np.float64)
+    lib().oracle_attention_bwd(_p(qf, C.c_float), _p(kf, C.c_float), _p(vf, C.c_float),
+                               _p(gf, C.c_float), _p(dq, C.c_double), _p(dk, C.c_double),
+                               _p(dv, C.c_double), B, Hh, N, d, float(scale), int(mask),
+                               int(window))
+    return dq, dk, dv
 
 
 def tile_visits(N: int, heads: int, mask: int, window: int, tile_q: int = 128,

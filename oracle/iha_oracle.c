@@ -36,6 +36,7 @@
  *     is (t / mu_w, t % mu_w) inside it; the grid is row-major.
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -277,6 +278,83 @@ void oracle_attention_rows(const float* q, const float* k, const float* v,
 /* [qi0 - kj1, qi1 - kj0]; it is visited iff that interval meets the visible */
 /* differences (>= 0 for causal, [0, window) for causal window, all for none).*/
 /* ------------------------------------------------------------------------ */
+/* ------------------------------------------------------------------------ */
+/* Attention backward (training step of the pseudo-head attention, the      */
+/* gradient of the forward above).  Dense tensors [B][N][Hh][d] (query and  */
+/* key sequences of one length N), dout as o.  Per (b, head) and query row i */
+/* with visible keys j, by the plain definitions:                            */
+/*   P_ij  = softmax_j(scale <q_i, k_j>)          (two-pass, max-shifted)     */
+/*   dV_j += P_ij dO_i                                                        */
+/*   dP_ij = <dO_i, v_j>                                                      */
+/*   D_i   = sum_j P_ij dP_ij                                                 */
+/*   dS_ij = P_ij (dP_ij - D_i)                                               */
+/*   dQ_i  = scale sum_j dS_ij k_j,   dK_j += scale dS_ij q_i                 */
+/* Heads are independent (parallel); inside a head the rows are summed in   */
+/* row order, so the result does not depend on scheduling.                  */
+/* ------------------------------------------------------------------------ */
+void oracle_attention_bwd(const float* q, const float* k, const float* v,
+                          const float* dout, double* dq, double* dk, double* dv,
+                          long B, long Hh, long N, long d, double scale,
+                          int mask, long window) {
+  const long row = Hh * d;  /* elements between consecutive tokens */
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+  for (long b = 0; b < B; ++b)
+    for (long h = 0; h < Hh; ++h) {
+      const long base = b * N * row + h * d;
+      double* P = (double*)malloc(sizeof(double) * (size_t)N);
+      double* dP = (double*)malloc(sizeof(double) * (size_t)N);
+      for (long j = 0; j < N; ++j)
+        for (long f = 0; f < d; ++f) {
+          dk[base + j * row + f] = 0.0;
+          dv[base + j * row + f] = 0.0;
+        }
+      for (long i = 0; i < N; ++i) {
+        const float* qi = q + base + i * row;
+        const float* gi = dout + base + i * row;
+        double m = -INFINITY;
+        for (long j = 0; j < N; ++j) {
+          if (!visible(i, j, mask, window)) { P[j] = -INFINITY; continue; }
+          const float* kj = k + base + j * row;
+          double dot = 0.0;
+          for (long f = 0; f < d; ++f) dot += (double)qi[f] * (double)kj[f];
+          P[j] = scale * dot;
+          if (P[j] > m) m = P[j];
+        }
+        double l = 0.0;
+        for (long j = 0; j < N; ++j) {
+          if (P[j] == -INFINITY) { P[j] = 0.0; continue; }
+          P[j] = exp(P[j] - m);
+          l += P[j];
+        }
+        double D = 0.0;
+        for (long j = 0; j < N; ++j) {
+          if (l > 0.0) P[j] /= l;
+          dP[j] = 0.0;
+          if (P[j] == 0.0) continue;
+          const float* vj = v + base + j * row;
+          for (long f = 0; f < d; ++f) dP[j] += (double)gi[f] * (double)vj[f];
+          D += P[j] * dP[j];
+        }
+        double* dqi = dq + base + i * row;
+        for (long f = 0; f < d; ++f) dqi[f] = 0.0;
+        for (long j = 0; j < N; ++j) {
+          if (P[j] == 0.0) continue;
+          const double ds = P[j] * (dP[j] - D);
+          const float* kj = k + base + j * row;
+          double* dkj = dk + base + j * row;
+          double* dvj = dv + base + j * row;
+          for (long f = 0; f < d; ++f) {
+            dqi[f] += scale * ds * (double)kj[f];
+            dkj[f] += scale * ds * (double)qi[f];
+            dvj[f] += P[j] * (double)gi[f];
+          }
+        }
+      }
+      free(P);
+      free(dP);
+    }
+}
+
 long oracle_tile_visits(long N, long heads, int mask, long window, long tile_q,
                         long tile_k) {
   long tq = (N + tile_q - 1) / tile_q, tk = (N + tile_k - 1) / tile_k;

@@ -414,3 +414,61 @@ def test_premix_pos0_rotates_by_absolute_position():
         a, b = m[0, n, :, 0], m[0, n, :, 1]
         np.testing.assert_allclose(y[0, n, :, 0], a * c - b * s, atol=1e-12)
         np.testing.assert_allclose(y[0, n, :, 1], b * c + a * s, atol=1e-12)
+
+
+# ----------------------------------------------------------------- attention backward
+def _bwd_inputs(B, N, Hh, d, seed):
+    """bf16-valued inputs: q +- 2^-12 * u (u in {-1, 0, 1}) stays exact in fp32."""
+    q, k, v, g = (S.bf16_bits_to_f32(S.normal((B, N, Hh, d), seed, c)) for c in range(4))
+    return q, k, v, g
+
+
+def _loss(q, k, v, g, mask, window):
+    o, _ = O.attention(q[:, None], k[:, None], v[:, None], mask, window)
+    return float(np.sum(o[:, 0] * g))
+
+
+@pytest.mark.parametrize("mask,window", [(0, 0), (1, 0), (2, 3)])
+def test_attention_bwd_matches_central_differences(mask, window):
+    """<grad, u> equals the central difference of L = <dO, O> along u, for
+    random sign directions u in q, k and v (the forward oracle is pinned on
+    its own); the step is exact in fp32 because the inputs are bf16 values."""
+    B, N, Hh, d = 1, 7, 2, 8
+    q, k, v, g = _bwd_inputs(B, N, Hh, d, 51 + mask)
+    dq, dk, dv = O.attention_bwd(q, k, v, g, mask, window)
+    rng = np.random.default_rng(9)
+    eps = 2.0 ** -12
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for _ in range(3):
+            u = rng.integers(-1, 2, size=x.shape).astype(np.float32)
+            xp, xm = x + np.float32(eps) * u, x - np.float32(eps) * u
+            args_p = dict(q=q, k=k, v=v)
+            args_m = dict(q=q, k=k, v=v)
+            args_p[name], args_m[name] = xp, xm
+            fd = (_loss(args_p["q"], args_p["k"], args_p["v"], g, mask, window) -
+                  _loss(args_m["q"], args_m["k"], args_m["v"], g, mask, window)) / (2 * eps)
+            an = float(np.sum(grad * u))
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, mask, fd, an)
+
+
+@pytest.mark.parametrize("mask,window", [(0, 0), (1, 0), (2, 5)])
+def test_attention_bwd_sums(mask, window):
+    """Sum over keys of dV equals the sum over queries of dO (each row of P
+    sums to 1); sum over keys of dK is 0 (shifting every key by one vector
+    adds a constant to each row's scores, which softmax ignores)."""
+    q, k, v, g = _bwd_inputs(2, 13, 3, 16, 61 + mask)
+    _, dk, dv = O.attention_bwd(q, k, v, g, mask, window)
+    np.testing.assert_allclose(dv.sum(axis=1), g.astype(np.float64).sum(axis=1), atol=1e-10)
+    np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-10)
+
+
+def test_attention_bwd_single_visible_key_has_no_query_gradient():
+    """A row that sees one key has a constant softmax: dQ = 0 there (causal
+    row 0, every row of window 1), and window 1 passes dO straight to dV."""
+    q, k, v, g = _bwd_inputs(1, 9, 2, 8, 71)
+    dq, _, _ = O.attention_bwd(q, k, v, g, 1, 0)
+    np.testing.assert_array_equal(dq[:, 0], 0.0)
+    dq, dk, dv = O.attention_bwd(q, k, v, g, 2, 1)
+    np.testing.assert_array_equal(dq, 0.0)
+    np.testing.assert_array_equal(dk, 0.0)
+    np.testing.assert_array_equal(dv, g.astype(np.float64))
