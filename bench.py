@@ -7,7 +7,8 @@ synthetic inputs, each at its workload's shape:
              for Q and K (fused RoPE, base 10000) and V; backward (input
              gradient, inverse RoPE for Q and K, and weight gradient from the
              same pass over dY) for Q, K, V;
-  attention  80 pseudo-heads, N=4096, d=128, causal window W=1024, fp32 LSE;
+  attention  80 pseudo-heads, N=4096, d=128, causal window W=1024, fp32 LSE,
+             and its backward (dQ, dK, dV for an upstream gradient dO);
   Hiera      MAE stage 1, B=128, 56x56 tokens, 8x8 units, 20 kept, C=d=96:
              gather, attention inside each unit, scatter;
   long ctx   the long-context IHA layer forward, B=2, N=16384, H=20, P=4,
@@ -88,9 +89,11 @@ def op_table():
     for t in "qkv":   # dX and dW from one read of dY and X
         ops.append((f"premix_bwd_{t}", y_b + 2 * x_b + 2 * w_b, 2 * pf))
     aw = S.LLAMA_WINDOW
-    ops.append(("attention_window",
-                4 * aw.B * aw.N * aw.HP * aw.d * 2 + aw.B * aw.HP * aw.N * 4,
-                4 * aw.d * _attn_pairs(aw.N, "window", S.WINDOW_KEYS) * aw.HP * aw.B))
+    attn_fl = 4 * aw.d * _attn_pairs(aw.N, "window", S.WINDOW_KEYS) * aw.HP * aw.B
+    tens = aw.B * aw.N * aw.HP * aw.d * 2
+    ops.append(("attention_window", 4 * tens + aw.B * aw.HP * aw.N * 4, attn_fl))
+    # backward: Q, K, V, O, dO and lse in, dQ, dK, dV out; five GEMMs to two
+    ops.append(("attention_window_bwd", 8 * tens + aw.B * aw.HP * aw.N * 4, attn_fl * 5 // 2))
     mu = S.HIERA_MU
     kept = mu.B * mu.n_keep * mu.unit_tokens * mu.C * 2
     ops.append(("mu_gather", 2 * kept + mu.B * mu.n_keep * 4, 0))
@@ -110,8 +113,9 @@ def op_table():
 
 def launches_per_step() -> int:
     # premix fwd 3; premix bwd 3 x (zero dW + kernel); window attention;
-    # gather, MU attention, scatter; long-context premix 3 + attention
-    return 3 + 3 * 2 + 1 + 3 + 3 + 1
+    # its backward (preprocess, kernel, postprocess); gather, MU attention,
+    # scatter; long-context premix 3 + attention
+    return 3 + 3 * 2 + 1 + 3 + 3 + 3 + 1
 
 
 def host_inputs(seed: int):
@@ -122,6 +126,7 @@ def host_inputs(seed: int):
         d[f"w_{t}"] = S.premix_weight(pm.H, pm.P, seed, 20 + c)
         d[f"dy_{t}"] = S.normal((pm.B, pm.N, pm.HP, pm.d), seed, 30 + c)
         d[f"a_{t}"] = S.normal((aw.B, aw.N, aw.HP, aw.d), seed, 40 + c)
+    d["a_do"] = S.normal((aw.B, aw.N, aw.HP, aw.d), seed, 43)
         d[f"lx_{t}"] = S.normal((lc.B, lc.N, lc.H, lc.d), seed, 60 + c)
         d[f"lw_{t}"] = S.premix_weight(lc.H, lc.P, seed, 70 + c)
     d["mu_x"] = S.normal((mu.B, mu.grid_h * mu.grid_w, mu.C), seed, 50)
@@ -161,6 +166,9 @@ class Step:
         self.dw = {t: e((pm.H, pm.P, pm.H), torch.float32) for t in "qkv"}
         self.o = e((aw.B, aw.N, aw.HP, aw.d))
         self.lse = e((aw.B, 1, aw.HP, aw.N), torch.float32)
+        self.agrad = {t: e((aw.B, aw.N, aw.HP, aw.d)) for t in "qkv"}
+        self.ws = torch.empty(T.mha_bwd_workspace_bytes(aw.B, aw.HP, aw.N, aw.d),
+                              dtype=torch.uint8, device=device)
         self.g = e((mu.B, mu.n_keep, mu.unit_tokens, mu.C))
         self.ou = e((mu.B, mu.n_keep, mu.unit_tokens, mu.C))
         self.dec = torch.zeros((mu.B, mu.grid_h * mu.grid_w, mu.C), dtype=torch.bfloat16,
@@ -173,7 +181,8 @@ class Step:
         """What a caller reads back: every op's final output (the long-context
         premix outputs are intermediates consumed by its attention)."""
         return ([self.y[t] for t in "qkv"] + [self.dx[t] for t in "qkv"] +
-                [self.dw[t] for t in "qkv"] + [self.o, self.lse, self.dec, self.lo, self.llse])
+                [self.dw[t] for t in "qkv"] + [self.o, self.lse] +
+                [self.agrad[t] for t in "qkv"] + [self.dec, self.lo, self.llse])
 
     def run(self, marks=None):
         """Enqueue the step; `marks(k)` records an event before op 0 and after op k-1."""
@@ -198,6 +207,10 @@ class Step:
             done()
         T.mha_fwd(i["a_q"], i["a_k"], i["a_v"], mask=T.MASK_CAUSAL_WINDOW, window=S.WINDOW_KEYS,
                   out=self.o, lse=self.lse)
+        done()
+        T.mha_bwd(i["a_q"], i["a_k"], i["a_v"], self.o, i["a_do"], self.lse,
+                  mask=T.MASK_CAUSAL_WINDOW, window=S.WINDOW_KEYS, dq=self.agrad["q"],
+                  dk=self.agrad["k"], dv=self.agrad["v"], workspace=self.ws)
         done()
         T.mu_gather(i["mu_x"], i["mu_keep"], mu.grid_h, mu.grid_w, mu.mu_h, mu.mu_w, out=self.g)
         done()
@@ -476,6 +489,10 @@ def oracle_sample(host, frac: float, seed: int = 0):
     n = max(1, int(n_all * frac))
     timed(lambda: attn_rows(host["a_q"], host["a_k"], host["a_v"], aw.HP, aw.N, aw.B,
                             O.MASK_CAUSAL_WINDOW, S.WINDOW_KEYS, n), n_all / n)
+    # backward: whole heads only (every key gathers over all its queries); one
+    # head stands in for the HP heads of every batch
+    h1 = [np.ascontiguousarray(host[nm][:1, :, :1]) for nm in ("a_q", "a_k", "a_v", "a_do")]
+    timed(lambda: O.attention_bwd(*h1, O.MASK_CAUSAL_WINDOW, S.WINDOW_KEYS), aw.HP * aw.B)
     nb = max(1, int(mu.B * frac))
     x, keep = host["mu_x"][:nb], host["mu_keep"][:nb]
 
@@ -504,8 +521,8 @@ def oracle_sample(host, frac: float, seed: int = 0):
     qa, ka, va = (np.ascontiguousarray(host[f"lx_{t}"][:, :, :1]) for t in "qkv")
     timed(lambda: attn_rows(qa, ka, va, 1, lc.N, lc.B, O.MASK_CAUSAL, 0, n), n_all / n)
     desc = (f"random {frac:.5f} of every op: tokens of each premix, query rows of each attention "
-            f"(uniform over batch, head, position), Hiera samples; each op's time scaled by "
-            f"its sampled share")
+            f"forward (uniform over batch, head, position), Hiera samples; one whole head of "
+            f"the attention backward; each op's time scaled by its sampled share")
     return t_full, t_meas, desc, O.num_threads()
 
 

@@ -39,6 +39,7 @@
 #ifndef IHA_H_
 #define IHA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -146,6 +147,33 @@ iha_status mha_fwd(const void* q, const void* k, const void* v, void* o,
                    int Nk, int d, iha_strides sq, iha_strides sk,
                    iha_strides sv, iha_strides so, float scale,
                    iha_mask mask_mode, int window, iha_dtype dt, void* stream);
+
+/*
+ * Attention backward over Hh heads ("Repository Structure": preprocess,
+ * backward, postprocess; "End-to-End Training Benchmark": the training step):
+ * with P = softmax(scale Q K^T | mask) recomputed from lse and dO the
+ * gradient of O = P V,
+ *   D_i = sum_f dO_if O_if,   dS = P o (dO V^T - D)
+ *   dq = scale dS K,   dk = scale dS^T Q,   dv = P^T dO.
+ *   q, k, v, o, dout   bf16 [B, N, Hh, d] dense (o, lse: the forward's outputs)
+ *   lse                float32 [B, Hh, N] (natural log, scale included)
+ *   dq, dk, dv         bf16 [B, N, Hh, d] dense, written; must not overlap
+ *                      each other, the inputs or the workspace
+ *   workspace          device scratch of at least mha_bwd_workspace_bytes()
+ *                      bytes, 256-byte aligned, owned by the caller: an fp32
+ *                      dQ accumulator and per-row D and lse * log2(e); its
+ *                      contents on entry do not matter and on return are
+ *                      unspecified
+ *   scale <= 0 selects 1/sqrt(d); mask_mode / window as mha_fwd (Nq = Nk = N).
+ * Needs bf16, d % 16 == 0, d <= 128.  Three launches on `stream`; dq gathers
+ * contributions with fp32 atomics, so its last bits depend on their order.
+ */
+size_t mha_bwd_workspace_bytes(int B, int Hh, int N, int d);
+iha_status mha_bwd(const void* q, const void* k, const void* v, const void* o,
+                   const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                   void* workspace, size_t workspace_bytes, int B, int Hh, int N,
+                   int d, float scale, iha_mask mask_mode, int window,
+                   iha_dtype dt, void* stream);
 
 /*
  * Mask-unit gather (README item 2, x[mask] -> gather):

@@ -48,7 +48,7 @@ def lib() -> C.CDLL:
                                        lp, lp, lp, d, i, l]
         L.oracle_attention_rows.argtypes = [fp, fp, fp, lp, l, dp, dp, l, l,
                                             lp, lp, lp, d, i, l]
-        L.oracle_attention_bwd.argtypes = [fp, fp, fp, fp, dp, dp, dp, l, l, l, l, d, i, l]
+        L.oracle_attention_bwd.argtypes = [fp, fp, fp, fp, dp, dp, dp, l, l, l, l, d, i, l, i]
         L.oracle_tile_visits.argtypes = [l, l, i, l, l, l]
         L.oracle_tile_visits.restype = l
         for name in ("oracle_mu_gather", "oracle_mu_scatter"):
@@ -180,9 +180,12 @@ def attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: np.ndarray
 
 
 def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,
-                  mask: int = 0, window: int = 0, scale: float | None = None):
+                  mask: int = 0, window: int = 0, scale: float | None = None,
+                  absolute: bool = False):
     """Gradients (dQ, dK, dV) of attention over dense [B, N, Hh, d] tensors
-    (float32 or bf16 bits) for the upstream gradient dout; float64 results."""
+    (float32 or bf16 bits) for the upstream gradient dout; float64 results.
+    absolute=True returns the same sums over absolute values of their terms
+    (sum |dS||k|, sum |dS||q|, sum P|dO|), the scale of rounding errors."""
     qf, kf, vf, gf = _as_f32(q), _as_f32(k), _as_f32(v), _as_f32(dout)
     B, N, Hh, d = qf.shape
     assert kf.shape == vf.shape == gf.shape == qf.shape
@@ -194,7 +197,7 @@ def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray,
     lib().oracle_attention_bwd(_p(qf, C.c_float), _p(kf, C.c_float), _p(vf, C.c_float),
                                _p(gf, C.c_float), _p(dq, C.c_double), _p(dk, C.c_double),
                                _p(dv, C.c_double), B, Hh, N, d, float(scale), int(mask),
-                               int(window))
+                               int(window), int(absolute))
     return dq, dk, dv
 
 

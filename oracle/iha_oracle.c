@@ -291,11 +291,14 @@ void oracle_attention_rows(const float* q, const float* k, const float* v,
 /*   dQ_i  = scale sum_j dS_ij k_j,   dK_j += scale dS_ij q_i                 */
 /* Heads are independent (parallel); inside a head the rows are summed in   */
 /* row order, so the result does not depend on scheduling.                  */
+/* With absolute != 0 the same sums are formed from absolute values of every */
+/* term (sum |dS||k|, sum |dS||q|, sum P |dO|): the magnitudes that bound     */
+/* rounding errors of an implementation that rounds dS and P.                */
 /* ------------------------------------------------------------------------ */
 void oracle_attention_bwd(const float* q, const float* k, const float* v,
                           const float* dout, double* dq, double* dk, double* dv,
                           long B, long Hh, long N, long d, double scale,
-                          int mask, long window) {
+                          int mask, long window, int absolute) {
   const long row = Hh * d;  /* elements between consecutive tokens */
 #pragma omp parallel for schedule(dynamic, 1) collapse(2)
   for (long b = 0; b < B; ++b)
@@ -343,6 +346,14 @@ void oracle_attention_bwd(const float* q, const float* k, const float* v,
           const float* kj = k + base + j * row;
           double* dkj = dk + base + j * row;
           double* dvj = dv + base + j * row;
+          if (absolute) {
+            for (long f = 0; f < d; ++f) {
+              dqi[f] += scale * fabs(ds) * fabs((double)kj[f]);
+              dkj[f] += scale * fabs(ds) * fabs((double)qi[f]);
+              dvj[f] += P[j] * fabs((double)gi[f]);
+            }
+            continue;
+          }
           for (long f = 0; f < d; ++f) {
             dqi[f] += scale * ds * (double)kj[f];
             dkj[f] += scale * ds * (double)qi[f];

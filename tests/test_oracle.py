@@ -472,3 +472,18 @@ def test_attention_bwd_single_visible_key_has_no_query_gradient():
     np.testing.assert_array_equal(dq, 0.0)
     np.testing.assert_array_equal(dk, 0.0)
     np.testing.assert_array_equal(dv, g.astype(np.float64))
+
+
+def test_attention_bwd_absolute_terms_bound_the_gradients():
+    """The absolute-term sums dominate the gradients element-wise and equal
+    them when every term has one sign (here: dV with dO >= 0)."""
+    q, k, v, g = _bwd_inputs(1, 11, 2, 8, 81)
+    for mask, window in ((0, 0), (1, 0), (2, 4)):
+        grads = O.attention_bwd(q, k, v, g, mask, window)
+        absg = O.attention_bwd(q, k, v, g, mask, window, absolute=True)
+        for a, b in zip(grads, absg):
+            assert np.all(np.abs(a) <= b * (1 + 1e-12) + 1e-300)
+    gp = np.abs(g)
+    _, _, dv = O.attention_bwd(q, k, v, gp, 1, 0)
+    _, _, av = O.attention_bwd(q, k, v, gp, 1, 0, absolute=True)
+    np.testing.assert_allclose(dv, av, rtol=1e-12)

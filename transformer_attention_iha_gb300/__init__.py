@@ -22,6 +22,7 @@ import os
 from . import _build
 
 __all__ = ["build", "lib", "premix_fwd", "premix_bwd_dx", "premix_bwd_dw", "premix_bwd", "mha_fwd",
+           "mha_bwd", "mha_bwd_workspace_bytes",
            "mu_gather", "mu_scatter", "device_error", "IHAError", "Strides", "MASK_NONE",
            "MASK_CAUSAL", "MASK_CAUSAL_WINDOW", "F32", "BF16"]
 
@@ -31,7 +32,7 @@ MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW = 0, 1, 2
 
 SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",
            "mha_fwd", "mu_gather", "mu_scatter", "iha_status_string", "iha_last_error",
-           "iha_device_error", "iha_test_fail_next_wait")
+           "iha_device_error", "iha_test_fail_next_wait", "mha_bwd", "mha_bwd_workspace_bytes")
 
 
 class IHAError(RuntimeError):
@@ -69,10 +70,14 @@ def lib() -> C.CDLL:
     L.iha_premix_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.mha_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, Strides, Strides, Strides,
                           Strides, f, i, i, i, vp]
+    L.mha_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    L.mha_bwd_workspace_bytes.restype = C.c_size_t
+    L.mha_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, C.c_size_t, i, i, i, i, f, i,
+                          i, i, vp]
     L.mu_gather.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     L.mu_scatter.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     for name in ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",
-                 "mha_fwd", "mu_gather", "mu_scatter"):
+                 "mha_fwd", "mha_bwd", "mu_gather", "mu_scatter"):
         getattr(L, name).restype = C.c_int
     L.iha_status_string.argtypes = [i]
     L.iha_status_string.restype = C.c_char_p
@@ -276,6 +281,43 @@ def mha_fwd(q, k, v, mask: int = MASK_NONE, window: int = 0, scale: float = 0.0,
                         float(scale), int(mask), int(window), _dt(q), _stream(stream)),
           "mha_fwd")
     return (out, lse) if return_lse else out
+
+
+def mha_bwd_workspace_bytes(B: int, Hh: int, N: int, d: int) -> int:
+    """Bytes of device scratch mha_bwd needs for [B, N, Hh, d] tensors."""
+    return int(lib().mha_bwd_workspace_bytes(B, Hh, N, d))
+
+
+def mha_bwd(q, k, v, o, dout, lse, mask: int = MASK_NONE, window: int = 0, scale: float = 0.0,
+            dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """(dQ, dK, dV) of attention over dense [B, N, Hh, d] bf16 tensors, given the
+    forward's output o and lse [B, Hh, N] (or [B, 1, Hh, N]) fp32 and the upstream
+    gradient dout.  `workspace` (uint8 CUDA tensor of mha_bwd_workspace_bytes) is
+    allocated here when not given."""
+    torch = _torch()
+    _expect(q, "q", dtype=torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, N, Hh, d]")
+    B, N, Hh, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _expect(t, name, (B, N, Hh, d), torch.bfloat16, q.device)
+    if lse.numel() != B * Hh * N:
+        raise ValueError(f"lse: {lse.numel()} elements, expected [B, Hh, N] = {(B, Hh, N)}")
+    _expect(lse, "lse", dtype=torch.float32, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _expect(t, name, (B, N, Hh, d), torch.bfloat16, q.device)
+    need = mha_bwd_workspace_bytes(B, Hh, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _expect(workspace, "workspace", dtype=torch.uint8, device=q.device)
+    check(lib().mha_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                        _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, Hh, N, d,
+                        float(scale), int(mask), int(window), _dt(q), _stream(stream)),
+          "mha_bwd")
+    return dq, dk, dv
 
 
 # ---------------------------------------------------------------- gather / scatter
