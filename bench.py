@@ -126,9 +126,9 @@ def host_inputs(seed: int):
         d[f"w_{t}"] = S.premix_weight(pm.H, pm.P, seed, 20 + c)
         d[f"dy_{t}"] = S.normal((pm.B, pm.N, pm.HP, pm.d), seed, 30 + c)
         d[f"a_{t}"] = S.normal((aw.B, aw.N, aw.HP, aw.d), seed, 40 + c)
-    d["a_do"] = S.normal((aw.B, aw.N, aw.HP, aw.d), seed, 43)
         d[f"lx_{t}"] = S.normal((lc.B, lc.N, lc.H, lc.d), seed, 60 + c)
         d[f"lw_{t}"] = S.premix_weight(lc.H, lc.P, seed, 70 + c)
+    d["a_do"] = S.normal((aw.B, aw.N, aw.HP, aw.d), seed, 43)
     d["mu_x"] = S.normal((mu.B, mu.grid_h * mu.grid_w, mu.C), seed, 50)
     d["mu_keep"] = S.keep_units(mu.B, mu.n_units, mu.n_keep, seed)
     return d
