@@ -176,6 +176,32 @@ iha_status mha_bwd(const void* q, const void* k, const void* v, const void* o,
                    iha_dtype dt, void* stream);
 
 /*
+ * Attention backward without any allocation.  The pages have no counterpart:
+ * this entry point exists for callers that cannot hand the library a device
+ * buffer and cannot call cudaMalloc themselves, for example a plugin inside a
+ * host program whose own allocator owns all device memory, or a code path
+ * that must not call cudaMalloc because it can synchronize the device.
+ * Same arguments and results as mha_bwd, minus the workspace: the scratch
+ * (fp32 dQ accumulator, per-row D and lse * log2(e)) lives in a 32 MiB array
+ * built into the library, which every GPU that loads the library keeps for
+ * the life of the process.
+ *   - Problems whose scratch exceeds 32 MiB (mha_bwd_workspace_bytes > 32 MiB,
+ *     e.g. B = 1, N = 4096, Hh = 8, d = 128 fits) are rejected with
+ *     IHA_ERR_UNSUPPORTED before anything is launched; use mha_bwd.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture on the device.
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     each call rewrites all of it that it reads, but calls that overlap on
+ *     the GPU (other streams, other host threads) race on it: serialize them.
+ */
+iha_status mha_bwd_noalloc(const void* q, const void* k, const void* v,
+                           const void* o, const void* dout, const float* lse,
+                           void* dq, void* dk, void* dv, int B, int Hh, int N,
+                           int d, float scale, iha_mask mask_mode, int window,
+                           iha_dtype dt, void* stream);
+
+/*
  * Mask-unit gather (README item 2, x[mask] -> gather):
  *   out[b,k,t,:] = x[b, tok(keep[b,k], t), :]
  * where the grid is row-major [grid_h, grid_w], mask units are mu_h x mu_w

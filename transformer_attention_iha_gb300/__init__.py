@@ -32,7 +32,8 @@ MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW = 0, 1, 2
 
 SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",
            "mha_fwd", "mu_gather", "mu_scatter", "iha_status_string", "iha_last_error",
-           "iha_device_error", "iha_test_fail_next_wait", "mha_bwd", "mha_bwd_workspace_bytes")
+           "iha_device_error", "iha_test_fail_next_wait", "mha_bwd", "mha_bwd_workspace_bytes",
+           "mha_bwd_noalloc")
 
 
 class IHAError(RuntimeError):
@@ -74,6 +75,8 @@ def lib() -> C.CDLL:
     L.mha_bwd_workspace_bytes.restype = C.c_size_t
     L.mha_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, C.c_size_t, i, i, i, i, f, i,
                           i, i, vp]
+    L.mha_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp]
+    L.mha_bwd_noalloc.restype = C.c_int
     L.mu_gather.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     L.mu_scatter.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     for name in ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",

@@ -687,3 +687,70 @@ iha_status mha_bwd(const void* q, const void* k, const void* v, const void* o, c
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free backward: the same three launches with the scratch in a
+// file-scope device array instead of a caller workspace.  The array is part
+// of the library image, so every GPU that loads the library holds it until
+// the process exits, and every call shares it.
+namespace iha {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;
+static __device__ __align__(256) uint8_t g_bwd_scratch[kNoAllocScratchBytes];
+
+// Device address of g_bwd_scratch per device: in host code the symbol is a
+// host-side stand-in, so it is looked up (once per device, with that device
+// current) and only the looked-up address is handed to kernels.
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+
+iha_status scratch_address(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(IHA_ERR_CUDA, "mha_bwd_noalloc: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(IHA_ERR_UNSUPPORTED, "mha_bwd_noalloc: device %d beyond %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
+    if (e != cudaSuccess || !ptr)
+      return fail(IHA_ERR_CUDA, "mha_bwd_noalloc: scratch address: %s",
+                  cudaGetErrorString(e));
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return IHA_OK;
+}
+
+}  // namespace
+}  // namespace iha
+
+extern "C" iha_status mha_bwd_noalloc(const void* q, const void* k, const void* v,
+                                      const void* o, const void* dout, const float* lse,
+                                      void* dq, void* dk, void* dv, int B, int Hh, int N, int d,
+                                      float scale, iha_mask mask_mode, int window, iha_dtype dt,
+                                      void* stream) {
+  using namespace iha;
+  iha_status st = mha_bwd_check("mha_bwd_noalloc", q, k, v, o, dout, lse, dq, dk, dv, B, Hh, N,
+                                d, mask_mode, window, dt);
+  if (st != IHA_OK) return st;
+  const size_t need = ws_layout(B, Hh, N, d).total;
+  if (need > kNoAllocScratchBytes)
+    return fail(IHA_ERR_UNSUPPORTED,
+                "mha_bwd_noalloc: this problem needs %zu bytes of scratch but the built-in "
+                "buffer holds %zu; call mha_bwd with a workspace instead",
+                need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  st = scratch_address(&scratch);
+  if (st != IHA_OK) return st;
+  if (mask_mode != IHA_MASK_CAUSAL_WINDOW) window = 0;
+  if (!(scale > 0.f)) scale = 1.f / sqrtf((float)d);
+  // the preprocess rewrites every scratch word this call reads (dQ
+  // accumulator zeroed, D and lse * log2(e) written), so the previous call's
+  // contents never leak into this one
+  return mha_bwd_launch(q, k, v, o, dout, lse, dq, dk, dv, scratch, B, Hh, N, d, scale,
+                        mask_mode, window, reinterpret_cast<cudaStream_t>(stream));
+}
