@@ -248,8 +248,9 @@ const char* iha_last_error(void);
 
 /*
  * Device error word of the current device: 0 if no kernel has flagged an
- * error, else a code (1 = out-of-range keep index, 2 = a bounded internal
- * wait gave up).  Synchronises the device; clears the word if clear != 0.
+ * error, else a bitwise OR of codes (1 = out-of-range keep index, 2 = a
+ * bounded internal wait gave up, 4 = a kernel found its dynamic shared memory
+ * not 1024-byte aligned and did nothing).  Synchronises the device; clears the word if clear != 0.
  * Returns -1 if the word cannot be read.
  */
 int iha_device_error(int clear);

@@ -20,11 +20,12 @@
 //                           P^T, dS^T by 4 compute warps (thread = key),
 //                           P in fp32 for dS (recomputed from S^T)
 //                           dV += P^T dO,  dK += dS^T Q        (TMEM)
-//                           dQ^T = K^T dS^T -> fp32 atomics into dQ_acc
+//                           dQ^T = K^T dS^T -> TMA reduce-add into dQ_acc
 //   attn_bwd_post_kernel  dQ = bf16(scale dQ_acc).
 // Roles of the main kernel (320 threads):
 //   warps 0-3  P^T and dS^T (thread = key row = TMEM lane), dK / dV epilogue
-//   warps 4-7  dQ^T drain (thread = feature = TMEM lane): coalesced atomics
+//   warps 4-7  dQ^T drain (thread = feature = TMEM lane): staged in the P / dS
+//              tile, added into dQ_acc by TMA reduce-add
 //   warp  8    TMA producer (K, V once per item; Q, dO per query tile, 2 stages)
 //   warp  9    tcgen05.mma issuer and TMEM owner
 // TMEM (512 columns): regions R0 | R1 rotate S^T / dP^T / dQ^T between query
@@ -47,9 +48,13 @@ constexpr int kB = 128;                      // keys (and queries) per tile
 constexpr int kChunkB = kB * 128;            // one 64-wide chunk of a 128-row tile (16 KB)
 constexpr int kTileB = 2 * kChunkB;          // a 128 x 128 bf16 tile (32 KB)
 constexpr int kThreads = 320;
-// shared memory: K | V | Q[2] | dO[2] | P/dS tiles, then barriers
+// shared memory: K | V | Q[2] | dO[2] | P/dS tiles | lse2, D per Q stage |
+// barriers.  No alignment slack fits: the dynamic shared memory must start
+// 1024-byte aligned (it does when the kernel has no static shared memory);
+// a kernel that finds otherwise reports DEV_ERR_SMEM_ALIGN and does nothing.
 constexpr int kSmemTiles = 7 * kTileB;
-constexpr int kSmemBytes = kSmemTiles + 256 + 1024;
+constexpr int kLDBytes = 2 * 2 * kB * 4;  // 2 stages x (lse2, D) x 128 floats
+constexpr int kSmemBytes = kSmemTiles + kLDBytes + 256;
 
 struct BwdParams {
   int B, Hh, N, d, Npad, ksteps, nch;
@@ -108,17 +113,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmDO, const BwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+                       const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0) {  // uniform: every thread leaves here
+    if (threadIdx.x == 0) atomicOr(&g_dev_error, DEV_ERR_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const uint32_t sK = smem_u32(smem);
   const uint32_t sV = sK + kTileB;
   const uint32_t sQ = sV + kTileB;           // 2 stages
   const uint32_t sDO = sQ + 2 * kTileB;      // 2 stages
   const uint32_t sPS = sDO + 2 * kTileB;     // P^T, then dS^T
   uint8_t* ps = smem + (sPS - sK);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemTiles);
+  const uint32_t sLD = sK + kSmemTiles;      // [stage][lse2 | D][128] fp32
+  const float* ld_f = reinterpret_cast<const float*>(smem + kSmemTiles);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemTiles + kLDBytes);
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t b_kvfull = bar0, b_kvempty = bar0 + 8u;
   auto b_qfull = [&](int s) { return bar0 + 8u * (2 + s); };
@@ -149,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_ptfull, 128);
     mbar_init(b_dvdone, 1);
     mbar_init(b_dsfull, 128);
-    mbar_init(b_psfree, 1);
+    mbar_init(b_psfree, 128);  // the four drain warps
     mbar_init(b_kvout, 1);
     mbar_init(b_kvoutempty, 128);
     mbar_init(b_drain, 1);
@@ -186,7 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int qt = it.qlo; qt <= it.qhi; ++qt, ++nq) {
           const int s = nq & 1;
           if (nq >= 2 && !(ok = mbar_wait(b_qempty(s), ((nq >> 1) - 1) & 1, abort_flag))) break;
-          mbar_arrive_expect_tx(b_qfull(s), 2 * tile_bytes);
+          mbar_arrive_expect_tx(b_qfull(s), 2 * tile_bytes + 2 * kB * 4);
+          const int64_t row0 = (int64_t)it.hb * p.Npad + qt * kB;  // 512-byte aligned
+          bulk_load(sLD + (uint32_t)s * 2 * kB * 4, p.lse2 + row0, kB * 4, b_qfull(s));
+          bulk_load(sLD + (uint32_t)s * 2 * kB * 4 + kB * 4, p.Dv + row0, kB * 4, b_qfull(s));
           for (int c = 0; c < p.nch; ++c) {
             tma_load_4d(sQ + s * kTileB + c * kChunkB, &tmQ, b_qfull(s), c * 64, qt * kB, it.h,
                         it.b);
@@ -274,7 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_ss_nm(tS, dka + (uint64_t)(kk * 128), dsb + (uint64_t)(kk * 128), id_dq,
                         kk > 0 ? 1u : 0u);
             mma_commit(b_dqfull(r));
-            mma_commit(b_psfree);
           }
         }
         if (!ok) break;
@@ -298,8 +311,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       int vis_hi = p.N - 1;
       if (p.mask == IHA_MASK_CAUSAL_WINDOW) vis_hi = min(vis_hi, kj + p.window - 1);
       const bool key_ok = kj < p.N;
-      const float* lse2_h = p.lse2 + (int64_t)it.hb * p.Npad;
-      const float* d_h = p.Dv + (int64_t)it.hb * p.Npad;
       for (int qt = it.qlo; qt <= it.qhi; ++qt, ++gt) {
         const int r = gt & 1;
         const uint32_t tS = tmem + lane_base + 128u * r, tP = tmem + lane_base + 128u * (r ^ 1);
@@ -307,7 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c_lo = key_ok ? max(vis_lo - q0, 0) : kB, c_hi = min(vis_hi - q0, kB - 1);
         // ---- P^T = exp2(s * scale_log2 - lse2) on visible (key, query) pairs
         if (!(ok = mbar_wait_warp(b_sfull, gt & 1, abort_flag))) break;
+        // this tile's lse2 and D have landed with its Q / dO stage
+        if (!(ok = mbar_wait_warp(b_qfull(gt & 1), (gt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
+        const float* lse2_s = ld_f + (gt & 1) * 2 * kB;
+        const float* d_s = lse2_s + kB;
         // the P / dS tile is free once the previous tile's dQ^T has read it
         if (gt >= 1 && !(ok = mbar_wait_warp(b_psfree, (gt - 1) & 1, abort_flag))) break;
 #pragma unroll 1
@@ -315,11 +330,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t sv[32];
           tmem_ld32(tS + 32u * c, sv);
           tmem_wait_ld();
-          const float4* l4 = reinterpret_cast<const float4*>(lse2_h + q0 + 32 * c);
+          const float4* l4 = reinterpret_cast<const float4*>(lse2_s + 32 * c);
           uint32_t pk[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 lv = __ldg(l4 + e4);
+            const float4 lv = l4[e4];
             const float lz[4] = {lv.x, lv.y, lv.z, lv.w};
             float pe[4];
 #pragma unroll
@@ -353,12 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tS + 32u * c, sv);
           tmem_ld32(tP + 32u * c, dp);
           tmem_wait_ld();
-          const float4* l4 = reinterpret_cast<const float4*>(lse2_h + q0 + 32 * c);
-          const float4* d4 = reinterpret_cast<const float4*>(d_h + q0 + 32 * c);
+          const float4* l4 = reinterpret_cast<const float4*>(lse2_s + 32 * c);
+          const float4* d4 = reinterpret_cast<const float4*>(d_s + 32 * c);
           uint32_t pw[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 lv = __ldg(l4 + e4), dv4 = __ldg(d4 + e4);
+            const float4 lv = l4[e4], dv4 = d4[e4];
             const float lz[4] = {lv.x, lv.y, lv.z, lv.w}, dz[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
             float ds[4];
 #pragma unroll
@@ -416,8 +431,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) raise_error(abort_flag);
   } else {
     // ------------------------------------------------------------ dQ^T drain (warps 4-7)
-    const int f = (warp - 4) * 32 + lane;  // feature = TMEM lane of dQ^T
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    // Warp wq stages its 32 features for 64 queries at a time (8 KB, fp32,
+    // rows of 32) in its quarter of the P / dS tile, free once dQ^T has read
+    // dS^T, and lane 0 adds the block into dQ_acc with one TMA reduce-add: the
+    // reduction runs in the bulk-copy engine, not as 16 K element atomics.
+    const int wq = warp - 4;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    float* stage = reinterpret_cast<float*>(ps + wq * 8192);
+    const uint32_t stage_s = sPS + (uint32_t)wq * 8192u;
+    const bool has_cols = wq * 32 < p.d;  // this warp's TMEM lanes hold real features
     bool ok = true;
     uint32_t gt = 0;
     for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
@@ -427,25 +449,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(b_dqfull(r), (gt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         const int q0 = qt * kB;
-        float* dst = p.dq_acc + (((int64_t)it.b * p.N + q0) * p.Hh + it.h) * p.d + f;
-        const int64_t qstride = (int64_t)p.Hh * p.d;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + 128u * r + 32u * c, v);
-          tmem_wait_ld();
-          if (f < p.d) {
+        for (int h = 0; h < 2; ++h) {  // queries 64h .. 64h + 63
+          if (h == 1) {
+            if (lane == 0) bulk_wait_read<0>();  // half 0's reduce has read the staging
+            __syncwarp();
+          }
+#pragma unroll 1
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + 128u * r + 32u * (2 * h + cc), v);
+            tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int qi = q0 + 32 * c + e;
-              if (qi < p.N) atomicAdd(dst + (int64_t)(32 * c + e) * qstride, __uint_as_float(v[e]));
-            }
+            for (int e = 0; e < 32; ++e) stage[(32 * cc + e) * 32 + lane] = __uint_as_float(v[e]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && has_cols && q0 + 64 * h < p.N) {
+            tma_reduce_add_4d(&tmDQ, stage_s, wq * 32, q0 + 64 * h, it.h, it.b);
+            bulk_commit();
           }
         }
         tc_fence_before();
-        mbar_arrive(b_dqempty(r));
+        mbar_arrive(b_dqempty(r));  // this TMEM region has been read
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        mbar_arrive(b_psfree);  // the staging (the P / dS tile) is free again
       }
     }
+    if (lane == 0) bulk_wait<0>();  // reductions complete before the CTA exits
     if (!ok) raise_error(abort_flag);
   }
 
@@ -563,7 +595,16 @@ iha_status mha_bwd_launch(const void* q, const void* k, const void* v, const voi
     const iha_status st = check_launch("mha_bwd (preprocess)");
     if (st != IHA_OK) return st;
   }
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
+  {
+    // dQ_acc [B, N, Hh, d] fp32, box 32 features x 64 queries, no swizzle
+    uint64_t dims[4] = {(uint64_t)d, (uint64_t)N, (uint64_t)Hh, (uint64_t)B};
+    uint64_t st[3] = {(uint64_t)Hh * d * 4, (uint64_t)d * 4, (uint64_t)N * Hh * d * 4};
+    uint32_t box[4] = {32, 64, 1, 1};
+    if (encode_tiled(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, st, box,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return fail(IHA_ERR_CUDA, "mha_bwd: dQ accumulator tensor map encoding failed");
+  }
   if (make_map4(&mq, q, B, N, Hh, d) != CUDA_SUCCESS ||
       make_map4(&mk, k, B, N, Hh, d) != CUDA_SUCCESS ||
       make_map4(&mv, v, B, N, Hh, d) != CUDA_SUCCESS ||
@@ -603,7 +644,7 @@ iha_status mha_bwd_launch(const void* q, const void* k, const void* v, const voi
     return fail(IHA_ERR_CUDA, "mha_bwd (smem attribute): %s", cudaGetErrorString(g_attr_err));
   int grid = sm_count();
   if (grid > p.n_items) grid = p.n_items;
-  attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);
   iha_status st = check_launch("mha_bwd");
   if (st != IHA_OK) return st;
   const int64_t n4 = (int64_t)B * N * Hh * d / 4;

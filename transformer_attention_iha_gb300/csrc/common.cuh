@@ -37,7 +37,7 @@ uint64_t wait_limit_for_next_launch();
 bool withhold_for_this_launch();
 
 // Device error codes (see iha_device_error in iha.h).
-enum : unsigned { DEV_ERR_KEEP_INDEX = 1u, DEV_ERR_WAIT_TIMEOUT = 2u };
+enum : unsigned { DEV_ERR_KEEP_INDEX = 1u, DEV_ERR_WAIT_TIMEOUT = 2u, DEV_ERR_SMEM_ALIGN = 4u };
 
 // Each translation unit owns one device error word (no relocatable device
 // code); its reader is registered here and iha_device_error() ORs them all.
@@ -175,6 +175,16 @@ __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int 
       "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// Tiled bulk reduce-add from shared memory into global (element type of the
+// tensor map; fp32 here), bulk-group completion like a store.
+__device__ __forceinline__ void tma_reduce_add_4d(const void* map, uint32_t src, int c0, int c1,
+                                                  int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit() {
