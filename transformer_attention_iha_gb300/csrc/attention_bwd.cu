@@ -18,14 +18,14 @@
 //                         tiles that see it (causal / window block skipping):
 //                           S^T  = K Q^T,  dP^T = V dO^T      (TMEM)
 //                           P^T, dS^T by 4 compute warps (thread = key),
-//                           P in fp32 for dS (recomputed from S^T)
+//                           fp32 P kept over S^T in TMEM for dS
 //                           dV += P^T dO,  dK += dS^T Q        (TMEM)
 //                           dQ^T = K^T dS^T -> TMA reduce-add into dQ_acc
 //   attn_bwd_post_kernel  dQ = bf16(scale dQ_acc).
 // Roles of the main kernel (320 threads):
 //   warps 0-3  P^T and dS^T (thread = key row = TMEM lane), dK / dV epilogue
-//   warps 4-7  dQ^T drain (thread = feature = TMEM lane): staged in the P / dS
-//              tile, added into dQ_acc by TMA reduce-add
+//   warps 4-7  dQ^T drain (thread = feature = TMEM lane): staged in the tile's
+//              Q / dO stage, added into dQ_acc by TMA reduce-add
 //   warp  8    TMA producer (K, V once per item; Q, dO per query tile, 2 stages)
 //   warp  9    tcgen05.mma issuer and TMEM owner
 // TMEM (512 columns): regions R0 | R1 rotate S^T / dP^T / dQ^T between query
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_kvempty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(b_qfull(s), 1);
-      mbar_init(b_qempty(s), 1);
+      mbar_init(b_qempty(s), 128);  // the drain warps release a Q / dO stage
       mbar_init(b_dqfull(s), 1);
       mbar_init(b_dqempty(s), 128);
     }
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_ptfull, 128);
     mbar_init(b_dvdone, 1);
     mbar_init(b_dsfull, 128);
-    mbar_init(b_psfree, 128);  // the four drain warps
+    mbar_init(b_psfree, 1);
     mbar_init(b_kvout, 1);
     mbar_init(b_kvoutempty, 128);
     mbar_init(b_drain, 1);
@@ -281,13 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_ss_nm(tDK, da + offa, db + (uint64_t)(kk * 128), id_acc,
                         (!first || kk > 0) ? 1u : 0u);
             }
-            mma_commit(b_qempty(s));  // Q and dO of this tile are no longer read
             const uint64_t dka = smem_desc_sw128(sK, kChunkB, 1024);
             const uint64_t dsb = smem_desc_sw128(sPS, kChunkB, 1024);
             for (int kk = 0; kk < kB / 16; ++kk)
               mma_ss_nm(tS, dka + (uint64_t)(kk * 128), dsb + (uint64_t)(kk * 128), id_dq,
                         kk > 0 ? 1u : 0u);
             mma_commit(b_dqfull(r));
+            mma_commit(b_psfree);  // dK and dQ^T have read dS^T
           }
         }
         if (!ok) break;
@@ -336,23 +336,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 lv = l4[e4];
             const float lz[4] = {lv.x, lv.y, lv.z, lv.w};
-            float pe[4];
+            float x[4], pe[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              x[u] = fmaf(__uint_as_float(sv[4 * e4 + u]), p.scale_log2, -lz[u]);
+            // a quarter of the exponentials on the FMA pipe
+            const float2 pp = (e4 & 1) ? exp2_poly3_x2(make_float2(x[2], x[3]))
+                                       : make_float2(fast_exp2(x[2]), fast_exp2(x[3]));
+            const float pv[4] = {fast_exp2(x[0]), fast_exp2(x[1]), pp.x, pp.y};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int col = 32 * c + 4 * e4 + u;
-              const float x = fmaf(__uint_as_float(sv[4 * e4 + u]), p.scale_log2, -lz[u]);
-              const float pv = fast_exp2(x);
-              pe[u] = (col >= c_lo && col <= c_hi) ? pv : 0.f;
+              pe[u] = (col >= c_lo && col <= c_hi) ? pv[u] : 0.f;
+              sv[4 * e4 + u] = __float_as_uint(pe[u]);  // fp32 P kept for dS
             }
             pk[2 * e4] = pack_bf16x2(pe[0], pe[1]);
             pk[2 * e4 + 1] = pack_bf16x2(pe[2], pe[3]);
           }
+          tmem_st32(tS + 32u * c, sv);  // P over S^T in TMEM
           // columns 32c .. 32c+31: chunk c / 2, granules 4 (c % 2) .. +3
 #pragma unroll
           for (int g = 0; g < 4; ++g)
             *reinterpret_cast<uint4*>(ps + swz(c >> 1, row, 4 * (c & 1) + g)) =
                 make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
         }
+        tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(b_ptfull);
@@ -362,27 +370,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          // P in fp32 again from S^T (still in TMEM until dQ^T replaces it):
-          // a bf16 P here would double the rounding error of dS
-          uint32_t sv[32], dp[32];
-          tmem_ld32(tS + 32u * c, sv);
+          // fp32 P (phase A left it over S^T in TMEM; a bf16 P here would
+          // double the rounding error of dS) and dP
+          uint32_t pv[32], dp[32];
+          tmem_ld32(tS + 32u * c, pv);
           tmem_ld32(tP + 32u * c, dp);
           tmem_wait_ld();
-          const float4* l4 = reinterpret_cast<const float4*>(lse2_s + 32 * c);
           const float4* d4 = reinterpret_cast<const float4*>(d_s + 32 * c);
           uint32_t pw[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 lv = l4[e4], dv4 = d4[e4];
-            const float lz[4] = {lv.x, lv.y, lv.z, lv.w}, dz[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
+            const float4 dv4 = d4[e4];
+            const float dz[4] = {dv4.x, dv4.y, dv4.z, dv4.w};
             float ds[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int col = 32 * c + 4 * e4 + u;
-              const float x = fmaf(__uint_as_float(sv[4 * e4 + u]), p.scale_log2, -lz[u]);
-              const float pf = (col >= c_lo && col <= c_hi) ? fast_exp2(x) : 0.f;
-              ds[u] = pf * (__uint_as_float(dp[4 * e4 + u]) - dz[u]);
-            }
+            for (int u = 0; u < 4; ++u)
+              ds[u] = __uint_as_float(pv[4 * e4 + u]) * (__uint_as_float(dp[4 * e4 + u]) - dz[u]);
             pw[2 * e4] = pack_bf16x2(ds[0], ds[1]);
             pw[2 * e4 + 1] = pack_bf16x2(ds[2], ds[3]);
           }
@@ -431,50 +434,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) raise_error(abort_flag);
   } else {
     // ------------------------------------------------------------ dQ^T drain (warps 4-7)
-    // Warp wq stages its 32 features for 64 queries at a time (8 KB, fp32,
-    // rows of 32) in its quarter of the P / dS tile, free once dQ^T has read
-    // dS^T, and lane 0 adds the block into dQ_acc with one TMA reduce-add: the
-    // reduction runs in the bulk-copy engine, not as 16 K element atomics.
+    // Once dQ^T(t) is complete, every MMA that reads tile t's Q / dO stage
+    // has finished, so the stage becomes the staging area: warp wq writes its
+    // 32 features for the 128 queries (16 KB, fp32, rows of 32) and lane 0
+    // adds them into dQ_acc with one TMA reduce-add (the reduction runs in the
+    // bulk-copy engine, not as 16 K element atomics); the warps then hand the
+    // stage back to the producer.
     const int wq = warp - 4;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    float* stage = reinterpret_cast<float*>(ps + wq * 8192);
-    const uint32_t stage_s = sPS + (uint32_t)wq * 8192u;
     const bool has_cols = wq * 32 < p.d;  // this warp's TMEM lanes hold real features
     bool ok = true;
     uint32_t gt = 0;
     for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
       const Item it = decode_item(p, idx);
       for (int qt = it.qlo; qt <= it.qhi; ++qt, ++gt) {
-        const int r = gt & 1;
+        const int r = gt & 1, s = gt & 1;
+        const uint32_t stage_s = (wq < 2 ? sQ : sDO) + (uint32_t)s * kTileB + (uint32_t)(wq & 1) * 16384u;
+        float* stage = reinterpret_cast<float*>(smem + (stage_s - sK));
         if (!(ok = mbar_wait_warp(b_dqfull(r), (gt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        const int q0 = qt * kB;
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {  // queries 64h .. 64h + 63
-          if (h == 1) {
-            if (lane == 0) bulk_wait_read<0>();  // half 0's reduce has read the staging
-            __syncwarp();
-          }
-#pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + 128u * r + 32u * (2 * h + cc), v);
-            tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + 128u * r + 32u * c, v);
+          tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) stage[(32 * cc + e) * 32 + lane] = __uint_as_float(v[e]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && has_cols && q0 + 64 * h < p.N) {
-            tma_reduce_add_4d(&tmDQ, stage_s, wq * 32, q0 + 64 * h, it.h, it.b);
-            bulk_commit();
-          }
+          for (int e = 0; e < 32; ++e) stage[(32 * c + e) * 32 + lane] = __uint_as_float(v[e]);
         }
         tc_fence_before();
         mbar_arrive(b_dqempty(r));  // this TMEM region has been read
-        if (lane == 0) bulk_wait_read<0>();
+        fence_proxy_async_smem();
         __syncwarp();
-        mbar_arrive(b_psfree);  // the staging (the P / dS tile) is free again
+        if (lane == 0) {
+          if (has_cols) {
+            tma_reduce_add_4d(&tmDQ, stage_s, wq * 32, qt * kB, it.h, it.b);
+            bulk_commit();
+          }
+          bulk_wait_read<0>();  // the reduce has read the staging
+        }
+        __syncwarp();
+        mbar_arrive(b_qempty(s));  // the stage is the producer's again
       }
     }
     if (lane == 0) bulk_wait<0>();  // reductions complete before the CTA exits
@@ -597,10 +596,10 @@ iha_status mha_bwd_launch(const void* q, const void* k, const void* v, const voi
   }
   CUtensorMap mq, mk, mv, mdo, mdq;
   {
-    // dQ_acc [B, N, Hh, d] fp32, box 32 features x 64 queries, no swizzle
+    // dQ_acc [B, N, Hh, d] fp32, box 32 features x 128 queries, no swizzle
     uint64_t dims[4] = {(uint64_t)d, (uint64_t)N, (uint64_t)Hh, (uint64_t)B};
     uint64_t st[3] = {(uint64_t)Hh * d * 4, (uint64_t)d * 4, (uint64_t)N * Hh * d * 4};
-    uint32_t box[4] = {32, 64, 1, 1};
+    uint32_t box[4] = {32, 128, 1, 1};
     if (encode_tiled(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, st, box,
                      CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
       return fail(IHA_ERR_CUDA, "mha_bwd: dQ accumulator tensor map encoding failed");
