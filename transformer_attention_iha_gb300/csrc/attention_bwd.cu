@@ -25,7 +25,7 @@
 // Roles of the main kernel (320 threads):
 //   warps 0-3  P^T and dS^T (thread = key row = TMEM lane), dK / dV epilogue
 //   warps 4-7  dQ^T drain (thread = feature = TMEM lane): staged in the tile's
-//              Q / dO stage, added into dQ_acc by TMA reduce-add
+//              Q / dO stage, added into dQ_acc by one TMA reduce-add a tile
 //   warp  8    TMA producer (K, V once per item; Q, dO per query tile, 2 stages)
 //   warp  9    tcgen05.mma issuer and TMEM owner
 // TMEM (512 columns): regions R0 | R1 rotate S^T / dP^T / dQ^T between query
@@ -123,9 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw;
   const uint32_t sK = smem_u32(smem);
   const uint32_t sV = sK + kTileB;
-  const uint32_t sQ = sV + kTileB;           // 2 stages
-  const uint32_t sDO = sQ + 2 * kTileB;      // 2 stages
-  const uint32_t sPS = sDO + 2 * kTileB;     // P^T, then dS^T
+  // 2 stages of Q | dO, each stage 64 KB contiguous (the dQ^T staging area)
+  const uint32_t sQ = sV + kTileB;           // Q of stage s at sQ + 2 s kTileB
+  const uint32_t sDO = sQ + kTileB;          // dO of stage s at sDO + 2 s kTileB
+  const uint32_t sPS = sQ + 4 * kTileB;      // P^T, then dS^T
   uint8_t* ps = smem + (sPS - sK);
   const uint32_t sLD = sK + kSmemTiles;      // [stage][lse2 | D][128] fp32
   const float* ld_f = reinterpret_cast<const float*>(smem + kSmemTiles);
@@ -139,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto b_dqfull = [&](int r) { return bar0 + 8u * (12 + r); };
   auto b_dqempty = [&](int r) { return bar0 + 8u * (14 + r); };
   const uint32_t b_kvout = bar0 + 8u * 16, b_kvoutempty = bar0 + 8u * 17;
-  const uint32_t b_drain = bar0 + 8u * 18;
+  const uint32_t b_drain = bar0 + 8u * 18, b_stg = bar0 + 8u * 19;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_kvempty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(b_qfull(s), 1);
-      mbar_init(b_qempty(s), 128);  // the drain warps release a Q / dO stage
+      mbar_init(b_qempty(s), 1);  // the dQ reduction has read the stage
       mbar_init(b_dqfull(s), 1);
       mbar_init(b_dqempty(s), 128);
     }
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_kvout, 1);
     mbar_init(b_kvoutempty, 128);
     mbar_init(b_drain, 1);
+    mbar_init(b_stg, 128);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -202,9 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load(sLD + (uint32_t)s * 2 * kB * 4, p.lse2 + row0, kB * 4, b_qfull(s));
           bulk_load(sLD + (uint32_t)s * 2 * kB * 4 + kB * 4, p.Dv + row0, kB * 4, b_qfull(s));
           for (int c = 0; c < p.nch; ++c) {
-            tma_load_4d(sQ + s * kTileB + c * kChunkB, &tmQ, b_qfull(s), c * 64, qt * kB, it.h,
+            tma_load_4d(sQ + 2 * s * kTileB + c * kChunkB, &tmQ, b_qfull(s), c * 64, qt * kB, it.h,
                         it.b);
-            tma_load_4d(sDO + s * kTileB + c * kChunkB, &tmDO, b_qfull(s), c * 64, qt * kB, it.h,
+            tma_load_4d(sDO + 2 * s * kTileB + c * kChunkB, &tmDO, b_qfull(s), c * 64, qt * kB, it.h,
                         it.b);
           }
         }
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int qt = it.qlo; ok && qt <= it.qhi; ++qt, ++gt) {
           const int s = gt & 1, r = gt & 1;
           const uint32_t tS = tmem + 128u * r, tP = tmem + 128u * (r ^ 1);
-          const uint32_t q_s = sQ + s * kTileB, do_s = sDO + s * kTileB;
+          const uint32_t q_s = sQ + 2 * s * kTileB, do_s = sDO + 2 * s * kTileB;
           if (!(ok = mbar_wait(b_qfull(s), (gt >> 1) & 1, abort_flag))) break;
           tc_fence_after();
           // S^T = K Q^T  (M = keys, N = queries, K = d)
@@ -435,21 +437,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ dQ^T drain (warps 4-7)
     // Once dQ^T(t) is complete, every MMA that reads tile t's Q / dO stage
-    // has finished, so the stage becomes the staging area: warp wq writes its
-    // 32 features for the 128 queries (16 KB, fp32, rows of 32) and lane 0
-    // adds them into dQ_acc with one TMA reduce-add (the reduction runs in the
-    // bulk-copy engine, not as 16 K element atomics); the warps then hand the
-    // stage back to the producer.
+    // has finished, so the stage (64 KB, contiguous) becomes the staging
+    // area: rows = queries, d fp32 features each, thread = feature writes its
+    // column.  When all 128 drain threads have written (b_stg), one thread
+    // adds the whole tile into dQ_acc with a single TMA reduce-add (box
+    // d x 128; the reduction runs in the bulk-copy engine, not as 16 K element
+    // atomics) and hands the stage back to the producer once it has been read.
     const int wq = warp - 4;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const bool has_cols = wq * 32 < p.d;  // this warp's TMEM lanes hold real features
+    const int feat = wq * 32 + lane;
+    const bool issuer = wq == 0 && lane == 0;
     bool ok = true;
     uint32_t gt = 0;
     for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
       const Item it = decode_item(p, idx);
       for (int qt = it.qlo; qt <= it.qhi; ++qt, ++gt) {
         const int r = gt & 1, s = gt & 1;
-        const uint32_t stage_s = (wq < 2 ? sQ : sDO) + (uint32_t)s * kTileB + (uint32_t)(wq & 1) * 16384u;
+        const uint32_t stage_s = sQ + 2u * (uint32_t)s * kTileB;
         float* stage = reinterpret_cast<float*>(smem + (stage_s - sK));
         if (!(ok = mbar_wait_warp(b_dqfull(r), (gt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
@@ -458,25 +462,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + 128u * r + 32u * c, v);
           tmem_wait_ld();
+          if (feat < p.d) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) stage[(32 * c + e) * 32 + lane] = __uint_as_float(v[e]);
+            for (int e = 0; e < 32; ++e) stage[(32 * c + e) * p.d + feat] = __uint_as_float(v[e]);
+          }
         }
         tc_fence_before();
         mbar_arrive(b_dqempty(r));  // this TMEM region has been read
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (has_cols) {
-            tma_reduce_add_4d(&tmDQ, stage_s, wq * 32, qt * kB, it.h, it.b);
+        mbar_arrive(b_stg);
+        if (issuer) {
+          if ((ok = mbar_wait(b_stg, gt & 1, abort_flag))) {
+            tma_reduce_add_4d(&tmDQ, stage_s, 0, qt * kB, it.h, it.b);
             bulk_commit();
+            bulk_wait_read<0>();     // the reduce has read the staging
+            mbar_arrive(b_qempty(s));  // the stage is the producer's again
           }
-          bulk_wait_read<0>();  // the reduce has read the staging
         }
-        __syncwarp();
-        mbar_arrive(b_qempty(s));  // the stage is the producer's again
+        if (wq == 0) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // warp-uniform
+        if (!ok) break;
       }
     }
-    if (lane == 0) bulk_wait<0>();  // reductions complete before the CTA exits
+    if (issuer) bulk_wait<0>();  // reductions complete before the CTA exits
     if (!ok) raise_error(abort_flag);
   }
 
@@ -596,10 +603,10 @@ iha_status mha_bwd_launch(const void* q, const void* k, const void* v, const voi
   }
   CUtensorMap mq, mk, mv, mdo, mdq;
   {
-    // dQ_acc [B, N, Hh, d] fp32, box 32 features x 128 queries, no swizzle
+    // dQ_acc [B, N, Hh, d] fp32, box d features x 128 queries, no swizzle
     uint64_t dims[4] = {(uint64_t)d, (uint64_t)N, (uint64_t)Hh, (uint64_t)B};
     uint64_t st[3] = {(uint64_t)Hh * d * 4, (uint64_t)d * 4, (uint64_t)N * Hh * d * 4};
-    uint32_t box[4] = {32, 128, 1, 1};
+    uint32_t box[4] = {(uint32_t)d, 128, 1, 1};
     if (encode_tiled(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, st, box,
                      CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
       return fail(IHA_ERR_CUDA, "mha_bwd: dQ accumulator tensor map encoding failed");
