@@ -54,10 +54,10 @@ UNIT = "% of 1-GPU roofline, summed over GPUs"
 # Fraction of every op the oracle runs per CPU sample (same in both CPU legs).
 CPU_FRAC = 1 / 256
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
-# capture summarised in profiles/ (None until a capture of the current kernel
-# exists; reset whenever that kernel changes).
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the dominant kernel, from the one-pass
+# ncu capture in profiles/attn_fwd_tc_causal_B2_N16384_80h_dram.md (removed
+# whenever that kernel changes, until it is captured again).
+NCU_TRAFFIC = {"long_attention_causal": 10743784960 + 673385216}
 
 
 def load_peaks():
@@ -118,20 +118,40 @@ def launches_per_step() -> int:
     return 3 + 3 * 2 + 1 + 3 + 3 + 3 + 1
 
 
-def host_inputs(seed: int):
+def _input_recipes(seed: int):
+    """Generator of every synthetic input of the step, by name."""
     pm, aw, mu, lc = S.LLAMA_PREMIX, S.LLAMA_WINDOW, S.HIERA_MU, S.LONG_CTX
-    d = {}
+    r = {}
     for c, t in enumerate("qkv"):
-        d[f"x_{t}"] = S.normal((pm.B, pm.N, pm.H, pm.d), seed, 10 + c)
-        d[f"w_{t}"] = S.premix_weight(pm.H, pm.P, seed, 20 + c)
-        d[f"dy_{t}"] = S.normal((pm.B, pm.N, pm.HP, pm.d), seed, 30 + c)
-        d[f"a_{t}"] = S.normal((aw.B, aw.N, aw.HP, aw.d), seed, 40 + c)
-        d[f"lx_{t}"] = S.normal((lc.B, lc.N, lc.H, lc.d), seed, 60 + c)
-        d[f"lw_{t}"] = S.premix_weight(lc.H, lc.P, seed, 70 + c)
-    d["a_do"] = S.normal((aw.B, aw.N, aw.HP, aw.d), seed, 43)
-    d["mu_x"] = S.normal((mu.B, mu.grid_h * mu.grid_w, mu.C), seed, 50)
-    d["mu_keep"] = S.keep_units(mu.B, mu.n_units, mu.n_keep, seed)
-    return d
+        r[f"x_{t}"] = lambda c=c: S.normal((pm.B, pm.N, pm.H, pm.d), seed, 10 + c)
+        r[f"w_{t}"] = lambda c=c: S.premix_weight(pm.H, pm.P, seed, 20 + c)
+        r[f"dy_{t}"] = lambda c=c: S.normal((pm.B, pm.N, pm.HP, pm.d), seed, 30 + c)
+        r[f"a_{t}"] = lambda c=c: S.normal((aw.B, aw.N, aw.HP, aw.d), seed, 40 + c)
+        r[f"lx_{t}"] = lambda c=c: S.normal((lc.B, lc.N, lc.H, lc.d), seed, 60 + c)
+        r[f"lw_{t}"] = lambda c=c: S.premix_weight(lc.H, lc.P, seed, 70 + c)
+    r["a_do"] = lambda: S.normal((aw.B, aw.N, aw.HP, aw.d), seed, 43)
+    r["mu_x"] = lambda: S.normal((mu.B, mu.grid_h * mu.grid_w, mu.C), seed, 50)
+    r["mu_keep"] = lambda: S.keep_units(mu.B, mu.n_units, mu.n_keep, seed)
+    return r
+
+
+def host_inputs(seed: int, keys=None):
+    rec = _input_recipes(seed)
+    return {k: rec[k]() for k in (keys if keys is not None else rec)}
+
+
+# inputs each op of the step reads (directly or through the op that feeds it)
+OP_INPUTS = {
+    **{f"premix_fwd_{t}": [f"x_{t}", f"w_{t}"] for t in "qkv"},
+    **{f"premix_bwd_{t}": [f"dy_{t}", f"x_{t}", f"w_{t}"] for t in "qkv"},
+    "attention_window": ["a_q", "a_k", "a_v"],
+    "attention_window_bwd": ["a_q", "a_k", "a_v", "a_do"],
+    "mu_gather": ["mu_x", "mu_keep"],
+    "mu_attention": ["mu_x", "mu_keep"],
+    "mu_scatter": ["mu_x", "mu_keep"],
+    **{f"long_premix_fwd_{t}": [f"lx_{t}", f"lw_{t}"] for t in "qkv"},
+    "long_attention_causal": [f"l{a}_{t}" for t in "qkv" for a in "xw"],
+}
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -558,6 +578,100 @@ def reference_arm(args, rank, world):
             "gpu_launches": 0}
 
 
+# --------------------------------------------------------------------------- one op
+def single_op(T, torch, name, dev, device):
+    """Enqueue function of one op of the step, on its full-size inputs only;
+    what feeds it (the forward before a backward, the gather before the MU
+    attention, the premix before the long-context attention) runs once here."""
+    pm, aw, mu, lc = S.LLAMA_PREMIX, S.LLAMA_WINDOW, S.HIERA_MU, S.LONG_CTX
+    e = lambda shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device=device)
+    i = dev
+    kind, t = name.rsplit("_", 1) if name[-2:] in ("_q", "_k", "_v") else (name, None)
+    if kind == "premix_fwd":
+        y = e((pm.B, pm.N, pm.HP, pm.d))
+        return lambda: T.premix_fwd(i[f"x_{t}"], i[f"w_{t}"], pm.P, rope=(t != "v"),
+                                    rope_base=S.ROPE_BASE, out=y)
+    if kind == "premix_bwd":
+        dx, dw = e((pm.B, pm.N, pm.H, pm.d)), e((pm.H, pm.P, pm.H), torch.float32)
+        return lambda: T.premix_bwd(i[f"dy_{t}"], i[f"x_{t}"], i[f"w_{t}"], rope=(t != "v"),
+                                    rope_base=S.ROPE_BASE, dx=dx, dw=dw)
+    if kind in ("attention_window", "attention_window_bwd"):
+        o, lse = e((aw.B, aw.N, aw.HP, aw.d)), e((aw.B, 1, aw.HP, aw.N), torch.float32)
+        fwd = lambda: T.mha_fwd(i["a_q"], i["a_k"], i["a_v"], mask=T.MASK_CAUSAL_WINDOW,
+                                window=S.WINDOW_KEYS, out=o, lse=lse)
+        if kind == "attention_window":
+            return fwd
+        fwd()
+        g = [e((aw.B, aw.N, aw.HP, aw.d)) for _ in range(3)]
+        ws = torch.empty(T.mha_bwd_workspace_bytes(aw.B, aw.HP, aw.N, aw.d), dtype=torch.uint8,
+                         device=device)
+        return lambda: T.mha_bwd(i["a_q"], i["a_k"], i["a_v"], o, i["a_do"], lse,
+                                 mask=T.MASK_CAUSAL_WINDOW, window=S.WINDOW_KEYS, dq=g[0],
+                                 dk=g[1], dv=g[2], workspace=ws)
+    if kind.startswith("mu_"):
+        g, ou = e((mu.B, mu.n_keep, mu.unit_tokens, mu.C)), e((mu.B, mu.n_keep, mu.unit_tokens, mu.C))
+        dec = torch.zeros((mu.B, mu.grid_h * mu.grid_w, mu.C), dtype=torch.bfloat16, device=device)
+        gather = lambda: T.mu_gather(i["mu_x"], i["mu_keep"], mu.grid_h, mu.grid_w, mu.mu_h,
+                                     mu.mu_w, out=g)
+        u = g.view(mu.B * mu.n_keep, 1, mu.unit_tokens, 1, mu.C)
+        attn = lambda: T.mha_fwd(u, u, u, out=ou.view(mu.B * mu.n_keep, 1, mu.unit_tokens, 1, mu.C))
+        scatter = lambda: T.mu_scatter(ou, i["mu_keep"], dec, mu.grid_h, mu.grid_w, mu.mu_h,
+                                       mu.mu_w)
+        if kind == "mu_gather":
+            return gather
+        gather()
+        if kind == "mu_attention":
+            return attn
+        attn()
+        return scatter
+    if kind == "long_premix_fwd":
+        ly = e((lc.B, lc.N, lc.HP, lc.d))
+        return lambda: T.premix_fwd(i[f"lx_{t}"], i[f"lw_{t}"], lc.P, rope=(t != "v"),
+                                    rope_base=S.ROPE_BASE, out=ly)
+    if kind == "long_attention_causal":
+        ly = {u: e((lc.B, lc.N, lc.HP, lc.d)) for u in "qkv"}
+        for u in "qkv":
+            T.premix_fwd(i[f"lx_{u}"], i[f"lw_{u}"], lc.P, rope=(u != "v"),
+                         rope_base=S.ROPE_BASE, out=ly[u])
+        lo, llse = e((lc.B, lc.N, lc.HP, lc.d)), e((lc.B, 1, lc.HP, lc.N), torch.float32)
+        return lambda: T.mha_fwd(ly["q"], ly["k"], ly["v"], mask=T.MASK_CAUSAL, out=lo, lse=llse)
+    raise ValueError(f"unknown op {name}")
+
+
+def single_op_arm(args):
+    """Time one op of the step alone (the case `ncu -k` captures): warm-up,
+    then `steps` launches between CUDA events on the launching stream."""
+    import torch
+    import transformer_attention_iha_gb300 as T
+    T.build()
+    T.lib()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    host = host_inputs(0, OP_INPUTS[args.only])
+    dev = {k: host_tensor(v, torch).to(device) for k, v in host.items()}
+    run = single_op(T, torch, args.only, dev, device)
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    if T.device_error() != 0:
+        raise RuntimeError("device error word set")
+    nbytes, flops = {n: (b, f) for n, b, f in op_table()}[args.only]
+    ms = e0.elapsed_time(e1) / args.steps
+    out = {"op": args.only, "ms": round(ms, 5), "GB/s": round(nbytes / ms / 1e6, 1),
+           "bytes": nbytes, "flops": flops, "steps": args.steps, "warmup": args.warmup,
+           "note": "back-to-back launches of one op (inputs may stay in L2); not the step metric"}
+    if flops:
+        out["TFLOP/s"] = round(flops / ms / 1e9, 1)
+    return out
+
+
 # --------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -572,6 +686,8 @@ def main():
     ap.add_argument("--cpu-samples", type=int, default=2,
                     help="oracle samples behind the cpu_baseline of the GPU arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=sorted(OP_INPUTS),
+                    help="time one op of the step alone on one GPU (profiling case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -582,6 +698,12 @@ def main():
     if args.gpus != world:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch N>1 with "
                  f"torch.distributed.run --nproc-per-node N")
+
+    if args.only:
+        if world != 1 or args.impl != "native":
+            ap.error("--only runs the native arm on one GPU")
+        print(json.dumps(single_op_arm(args)), flush=True)
+        return
 
     if args.impl == "reference":
         line = reference_arm(args, rank, world)
