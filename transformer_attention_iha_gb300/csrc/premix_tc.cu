@@ -49,7 +49,9 @@ struct FwdParams {
 // cos / sin of n * inv_freq with inv_freq = hi + lo (fp32 pair).  The product
 // is carried as p + c (p = fl(n*hi), c = exact error + n*lo) and reduced
 // modulo 2*pi by an FMA-based Cody-Waite step (2*pi split into fp32 hi + lo),
-// keeping the reduced angle accurate to ~3e-7 for positions up to 2^24.
+// keeping the reduced angle accurate to ~3e-7 for positions up to 2^24.  On
+// the reduced angle (|r| <= pi + 1e-6) the hardware sine / cosine is accurate
+// to ~2^-21 absolute, far below the bf16 rounding of the rotated values.
 __device__ __forceinline__ void rope_cos_sin(int n, float hi, float lo, float& c, float& s) {
   const float nf = (float)n;
   const float p = nf * hi;
@@ -58,7 +60,17 @@ __device__ __forceinline__ void rope_cos_sin(int n, float hi, float lo, float& c
   float r = fmaf(-k, 6.2831854820251465f, p);
   r = fmaf(-k, -1.7484555314695172e-07f, r);
   r += corr;
-  sincosf(r, &s, &c);
+  __sincosf(r, &s, &c);
+}
+
+// inv_freq (hi, lo) of pair i, read with static indices only: a lane-dependent
+// index into the by-value parameter block would go through local memory.
+__device__ __forceinline__ float2 rope_inv_freq(const RopeTable& rt, int i) {
+  float2 r = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < 64; ++k)
+    if (k == i) r = make_float2(rt.hi[k], rt.lo[k]);
+  return r;
 }
 
 __device__ __forceinline__ void raise_error(volatile int* abort_flag) {
@@ -79,8 +91,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sW = smem_u32(smem);                      // 16 KB
   const uint32_t sX = sW + 16384;                          // kXStages x stage_bytes
   const uint32_t sStage = sX + kXStages * p.stage_bytes;   // 8 warps x kWarpStage
-  float2* rope_tabs = reinterpret_cast<float2*>(smem + (sStage - sW) + 8 * kWarpStage);  // [8][64]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rope_tabs + 8 * 64);
+  // per epilogue warp: cos / sin of its token, [HALF / 2] x (c_2j, c_2j+1, s_2j, s_2j+1)
+  float4* rope_tabs = reinterpret_cast<float4*>(smem + (sStage - sW) + 8 * kWarpStage);  // [8][32]
+  float2* inv_tab = reinterpret_cast<float2*>(rope_tabs + 8 * 32);  // [64] inv_freq (hi, lo)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(inv_tab + 64);
   const uint32_t bar0 = smem_u32(bars);
   auto b_xfull = [&](int s) { return bar0 + 8u * s; };
   auto b_xempty = [&](int s) { return bar0 + 8u * (kXStages + s); };
@@ -104,6 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_drain, 1);
     *abort_flag = 0;
     mbar_init_fence();
+#pragma unroll
+    for (int i = 0; i < 64; ++i) inv_tab[i] = make_float2(p.rt.hi[i], p.rt.lo[i]);
   }
   // W -> bf16 hi | lo, K-major rows of 64 (hi s0..31 | lo s0..31), 128B swizzle
   if (tid < kEpiThreads) {
@@ -192,61 +208,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool warp_active = q * 32 < p.HP;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const uint32_t wstage = sStage + (uint32_t)warp * kWarpStage;
-    float2* tab = rope_tabs + warp * 64;
+    float4* tab = rope_tabs + warp * 32;
     int k = 0;
     for (int g = blockIdx.x; g < p.n_stages; g += gridDim.x, ++k) {
       const int a = k & 1, sb = k & 1;
       const int t = g * kTok + tt;
-      if (p.rope && warp_active) {
-        for (int i = lane; i < HALF; i += 32) {
-          float c, sn;
-          rope_cos_sin(t % p.N, p.rt.hi[i], p.rt.lo[i], c, sn);
-          tab[i] = make_float2(c, sn);
-        }
+      if (p.rope && warp_active && 2 * lane < HALF) {
+        float c0, s0, c1, s1;
+        const float4 inv = reinterpret_cast<const float4*>(inv_tab)[lane];  // pairs 2 lane, 2 lane + 1
+        rope_cos_sin(t % p.N, inv.x, inv.y, c0, s0);
+        rope_cos_sin(t % p.N, inv.z, inv.w, c1, s1);
+        tab[lane] = make_float4(c0, c1, s0, s1);
       }
       __syncwarp();
       // after an abort: no TMEM loads and no stores, only the arrivals
       const bool live = mbar_wait_warp(b_accfull(a), (k >> 1) & 1, abort_flag);
       if (!live) raise_error(abort_flag);
       tc_fence_after();
-      float v[D];
-      if (warp_active && live) {
-        const uint32_t col = tmem + lane_base + (uint32_t)(a * 256 + tt * D);
-#pragma unroll
-        for (int c = 0; c < 2 * NCH; ++c) tmem_ld32(col + 32u * c, reinterpret_cast<uint32_t*>(v) + 32 * c);
-        tmem_wait_ld();
-      }
-      tc_fence_before();
-      mbar_arrive(b_accempty(a));
-      if (!live) break;
-      if (warp_active && t < p.ntok) {
+      // Two passes over the accumulator: pass hh holds columns 32 hh .. +31
+      // and their RoPE partners HALF + 32 hh .. +31 (64 registers, not D).
+      const uint32_t col = tmem + lane_base + (uint32_t)(a * 256 + tt * D);
+      const bool work = warp_active && live && t < p.ntok;
+      if (work) {
         if (lane == 0) bulk_wait_read<1>();  // this warp's buffer sb is free again
         __syncwarp();
-        if (row < p.HP) {
-          if (p.rope) {
+      }
 #pragma unroll
-            for (int i = 0; i < HALF; ++i) {
-              const float2 cs = tab[i];
-              const float x0 = v[i], x1 = v[i + HALF];
-              v[i] = fmaf(x0, cs.x, -x1 * cs.y);
-              v[i + HALF] = fmaf(x1, cs.x, x0 * cs.y);
+      for (int hh = 0; hh < HALF / 32; ++hh) {
+        float v[64];
+        if (work) {
+          tmem_ld32(col + 32u * hh, reinterpret_cast<uint32_t*>(v));
+          tmem_ld32(col + (uint32_t)HALF + 32u * hh, reinterpret_cast<uint32_t*>(v) + 32);
+          tmem_wait_ld();
+        }
+        if (hh == HALF / 32 - 1) {  // every column has been read
+          tc_fence_before();
+          mbar_arrive(b_accempty(a));
+        }
+        if (work && row < p.HP) {
+          if (p.rope) {
+            // pairs (i, i + HALF) two at a time on the packed fp32 pipe
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float4 cs = tab[16 * hh + j];
+              const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
+              const float2 x0 = make_float2(v[2 * j], v[2 * j + 1]);
+              const float2 x1 = make_float2(v[32 + 2 * j], v[32 + 2 * j + 1]);
+              const float2 y0 = __ffma2_rn(x0, c2, __fmul2_rn(make_float2(-x1.x, -x1.y), s2));
+              const float2 y1 = __ffma2_rn(x0, s2, __fmul2_rn(x1, c2));
+              v[2 * j] = y0.x;
+              v[2 * j + 1] = y0.y;
+              v[32 + 2 * j] = y1.x;
+              v[32 + 2 * j + 1] = y1.y;
             }
           }
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            uint8_t* blk = smem + (wstage - sW) + (uint32_t)(sb * NCH + c) * 4096u + lane * 128;
+          for (int part = 0; part < 2; ++part) {
+            const int c0 = part ? HALF + 32 * hh : 32 * hh;  // first column of the part
+            uint8_t* blk = smem + (wstage - sW) + (uint32_t)(sb * NCH + c0 / 64) * 4096u + lane * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int f = 64 * c + 8 * j;
+            for (int g = 0; g < 4; ++g) {
+              const int j = (c0 % 64) / 8 + g;  // 16-byte granule of the 128-byte row
+              const float* vv = v + 32 * part + 8 * g;
               uint4 u;
-              u.x = pack_bf16x2(v[f + 0], v[f + 1]);
-              u.y = pack_bf16x2(v[f + 2], v[f + 3]);
-              u.z = pack_bf16x2(v[f + 4], v[f + 5]);
-              u.w = pack_bf16x2(v[f + 6], v[f + 7]);
+              u.x = pack_bf16x2(vv[0], vv[1]);
+              u.y = pack_bf16x2(vv[2], vv[3]);
+              u.z = pack_bf16x2(vv[4], vv[5]);
+              u.w = pack_bf16x2(vv[6], vv[7]);
               *reinterpret_cast<uint4*>(blk + ((j ^ (lane & 7)) << 4)) = u;
             }
           }
         }
+      }
+      if (!live) break;
+      if (work) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -320,7 +355,7 @@ iha_status premix_fwd_tc(const void* x, const float* w, void* y, int B, int N, i
       return fail(IHA_ERR_CUDA, "iha_premix_fwd: Y tensor map encoding failed");
   }
   const size_t smem = 1024 + 16384 + kXStages * p.stage_bytes + 8 * 2 * p.nch * 4096 +
-                      8 * 64 * sizeof(float2) + 256;
+                      8 * 32 * sizeof(float4) + 64 * sizeof(float2) + 256;
   auto kern = d == 128 ? premix_fwd_tc_kernel<128> : premix_fwd_tc_kernel<64>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
@@ -583,6 +618,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (PREP) {
       const int u = tid - 320;  // 0..63
       float2* tab = reinterpret_cast<float2*>(gen(sRope));
+      const float2 inv = rope_inv_freq(p.rt, u);
       for (int k = 0; k < n_my; ++k) {
         const int tok = blockIdx.x + k * gridDim.x, s = k % NS;
         const uint32_t xs = sStages + (uint32_t)s * p.stage_bytes + p.dy_bytes;
@@ -590,7 +626,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         named_bar_sync(1, 64);  // the previous token's table reads are done
         {
           float c, sn;
-          rope_cos_sin(tok % p.N, p.rt.hi[u], p.rt.lo[u], c, sn);
+          rope_cos_sin(tok % p.N, inv.x, inv.y, c, sn);
           tab[u] = make_float2(c, sn);
         }
         named_bar_sync(1, 64);
@@ -665,6 +701,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(b_dwempty(b));
     };
+    const float2 inv = ROPE ? rope_inv_freq(p.rt, f & 63) : make_float2(0.f, 0.f);
     const int n_dwc = (n_my + kDwChunk - 1) / kDwChunk;
     int dwc_done = 0;
     int it = 0;
@@ -676,7 +713,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int tok = blockIdx.x + k * gridDim.x;
         const int a = k % kBwdNA;
         float c = 1.f, sn = 0.f;
-        if (ROPE) rope_cos_sin(tok % p.N, p.rt.hi[f & 63], p.rt.lo[f & 63], c, sn);
+        if (ROPE) rope_cos_sin(tok % p.N, inv.x, inv.y, c, sn);
         const bool live = ok && mbar_wait_warp(b_accfull(a), (k / kBwdNA) & 1, abort_flag);
         if (ok && !live) {
           ok = false;
