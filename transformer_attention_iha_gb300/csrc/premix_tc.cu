@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sEx = sOut + out_total;
   const uint32_t ex_total = EXCH ? 16u * p.ex_bytes : 0u;
   const uint32_t sRope = sEx + ex_total;
-  const uint32_t rope_bytes = PREP ? 64u * 8u : 0u;
+  const uint32_t rope_bytes = PREP ? 2u * 32u * 16u : 0u;  // 2 tokens x [32] float4
   auto gen = [&](uint32_t a) { return smem + (a - sWT); };  // shared address -> pointer
   uint64_t* bars = reinterpret_cast<uint64_t*>(gen((sRope + rope_bytes + 7u) & ~7u));
   const uint32_t bar0 = smem_u32(bars);
@@ -568,21 +568,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t idesc_dx = idesc_bf16_f32(128, 64, true, false);
       const uint32_t idesc_dw = idesc_bf16_f32(128, NDW, false, false);
       const int nk_hp = p.hp_pad >> 4;
+      // Descriptors of stage 0 / K-step 0; a K-step or a stage adds its byte
+      // offset >> 4 to the start-address field (no carry: every operand lies
+      // in the first 256 KB of shared memory).
+      const uint64_t d_dx_a = smem_desc_sw128(sStages, p.chunk, 1024);  // dY, MN-major
+      const uint64_t d_dx_b = smem_desc_sw128(sWT, 16, 1024);           // W^T hi | lo
+      const uint64_t d_dw_a = smem_desc_sw128(sStages, 16, 1024);       // dY, K-major
+      const uint64_t d_dw_b = PREP ? smem_desc_sw128(sXr, 16, 1024)
+                                   : smem_desc_sw128(sStages + p.dy_bytes, 16, 1024);
+      const uint32_t xchunk = PREP ? 8192u : 4096u;
+      const uint32_t chunk = p.chunk, stage_bytes = p.stage_bytes;
       bool ok = true;
       for (int k = 0; k < n_my; ++k) {
         const int s = k % NS;
-        const uint32_t st = sStages + (uint32_t)s * p.stage_bytes;
+        const uint64_t st16 = (uint64_t)(((uint32_t)s * stage_bytes) >> 4);
         if (!(ok = mbar_wait(b_infull(s), (k / NS) & 1, abort_flag))) break;
         tc_fence_after();
         if (DO_DX) {
           const int a = k % kBwdNA;
           if (!(ok = mbar_wait(b_accempty(a), ((k / kBwdNA) & 1) ^ 1, abort_flag))) break;
           tc_fence_after();
-          for (int kk = 0; kk < nk_hp; ++kk) {
-            const uint32_t bw = sWT + (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
-            mma_ss(tmem + (uint32_t)(a * 64), smem_desc_sw128(st + (uint32_t)kk * 2048u, p.chunk, 1024),
-                   smem_desc_sw128(bw, 16, 1024), idesc_dx, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < nk_hp; ++kk)
+            mma_ss_nm(tmem + (uint32_t)(a * 64), d_dx_a + st16 + (uint64_t)(kk * 128),
+                      d_dx_b + (uint64_t)((((kk >> 2) * 8192) + (kk & 3) * 32) >> 4), idesc_dx,
+                      kk > 0 ? 1u : 0u);
           mma_commit(b_accfull(a));
         }
         if (DO_DW) {
@@ -590,20 +599,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const bool dw_first = (k % kDwChunk) == 0;
           if (dw_first && dwc >= 2 &&
               !(ok = mbar_wait(b_dwempty(dwb), ((dwc >> 1) - 1) & 1, abort_flag))) break;
-          uint32_t xsrc = st + p.dy_bytes;
-          uint32_t xchunk = 4096u;
+          uint64_t xb = d_dw_b + st16;
           if (PREP) {
             if (!(ok = mbar_wait(b_xrfull(k & 1), (k >> 1) & 1, abort_flag))) break;
             tc_fence_after();
-            xsrc = sXr + (uint32_t)(k & 1) * 16384u;
-            xchunk = 8192u;
+            xb = d_dw_b + (uint64_t)((k & 1) * (16384 >> 4));
           }
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t aoff = (uint32_t)(kk >> 2) * p.chunk + (uint32_t)(kk & 3) * 32u;
+            const uint32_t aoff = (uint32_t)(kk >> 2) * chunk + (uint32_t)(kk & 3) * 32u;
             const uint32_t boff = (uint32_t)(kk >> 2) * xchunk + (uint32_t)(kk & 3) * 32u;
-            mma_ss(tmem_dw + (uint32_t)(64 * dwb), smem_desc_sw128(st + aoff, 16, 1024),
-                   smem_desc_sw128(xsrc + boff, 16, 1024), idesc_dw,
-                   (!dw_first || kk > 0) ? 1u : 0u);
+            mma_ss_nm(tmem_dw + (uint32_t)(64 * dwb), d_dw_a + st16 + (uint64_t)(aoff >> 4),
+                      xb + (uint64_t)(boff >> 4), idesc_dw, (!dw_first || kk > 0) ? 1u : 0u);
           }
           if (PREP) mma_commit(b_xrempty(k & 1));
           if ((k % kDwChunk) == kDwChunk - 1 || k == n_my - 1) mma_commit(b_dwfull(dwb));
@@ -617,21 +624,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ R X (hi / lo)
     if (PREP) {
       const int u = tid - 320;  // 0..63
-      float2* tab = reinterpret_cast<float2*>(gen(sRope));
+      // cos / sin of the token, double-buffered: [32] x (c_2m, c_2m+1, s_2m, s_2m+1)
+      float* tabs = reinterpret_cast<float*>(gen(sRope));
       const float2 inv = rope_inv_freq(p.rt, u);
       for (int k = 0; k < n_my; ++k) {
         const int tok = blockIdx.x + k * gridDim.x, s = k % NS;
         const uint32_t xs = sStages + (uint32_t)s * p.stage_bytes + p.dy_bytes;
         const uint32_t xr = sXr + (uint32_t)(k & 1) * 16384u;
-        named_bar_sync(1, 64);  // the previous token's table reads are done
+        float* tw = tabs + (k & 1) * 128;
         {
           float c, sn;
           rope_cos_sin(tok % p.N, inv.x, inv.y, c, sn);
-          tab[u] = make_float2(c, sn);
+          tw[4 * (u >> 1) + (u & 1)] = c;
+          tw[4 * (u >> 1) + 2 + (u & 1)] = sn;
         }
+        // the table is complete (and buffer k & 1 was last read two tokens ago)
         named_bar_sync(1, 64);
         if (!mbar_wait(b_infull(s), (k / NS) & 1, abort_flag)) raise_error(abort_flag);
         if (!mbar_wait(b_xrempty(k & 1), ((k >> 1) & 1) ^ 1, abort_flag)) raise_error(abort_flag);
+        const float4* t4 = reinterpret_cast<const float4*>(tw);
         for (int task = u; task < p.H * 8; task += 64) {
           const int j = task / p.H, row = task - j * p.H;  // neighbours share j: table broadcast
           const uint32_t off = (uint32_t)row * 128u + (uint32_t)((j ^ (row & 7)) << 4);
@@ -642,19 +653,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t ah[4], al[4], bh[4], bl[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float ra[2], rb[2];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const float x0 = h2 ? bf16hi_to_f32(av[e]) : bf16lo_to_f32(av[e]);
-              const float x1 = h2 ? bf16hi_to_f32(bv[e]) : bf16lo_to_f32(bv[e]);
-              const float2 cs = tab[8 * j + 2 * e + h2];
-              ra[h2] = fmaf(x0, cs.x, -x1 * cs.y);
-              rb[h2] = fmaf(x1, cs.x, x0 * cs.y);
-            }
-            ah[e] = pack_bf16x2(ra[0], ra[1]);
-            bh[e] = pack_bf16x2(rb[0], rb[1]);
-            al[e] = pack_bf16x2(ra[0] - bf16lo_to_f32(ah[e]), ra[1] - bf16hi_to_f32(ah[e]));
-            bl[e] = pack_bf16x2(rb[0] - bf16lo_to_f32(bh[e]), rb[1] - bf16hi_to_f32(bh[e]));
+            // features 8j + 2e, +1 (x0) and their partners 64 + 8j + 2e, +1 (x1)
+            const float4 cs = t4[4 * j + e];
+            const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
+            const float2 x0 = make_float2(bf16lo_to_f32(av[e]), bf16hi_to_f32(av[e]));
+            const float2 x1 = make_float2(bf16lo_to_f32(bv[e]), bf16hi_to_f32(bv[e]));
+            const float2 ra = __ffma2_rn(x0, c2, __fmul2_rn(make_float2(-x1.x, -x1.y), s2));
+            const float2 rb = __ffma2_rn(x0, s2, __fmul2_rn(x1, c2));
+            ah[e] = pack_bf16x2(ra.x, ra.y);
+            bh[e] = pack_bf16x2(rb.x, rb.y);
+            al[e] = pack_bf16x2(ra.x - bf16lo_to_f32(ah[e]), ra.y - bf16hi_to_f32(ah[e]));
+            bl[e] = pack_bf16x2(rb.x - bf16lo_to_f32(bh[e]), rb.y - bf16hi_to_f32(bh[e]));
           }
           // box c of a slot: 64 rows (hi rows 0..31, lo rows 32..63) x 128 B
           *reinterpret_cast<uint4*>(gen(xr + off)) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
@@ -814,7 +823,7 @@ bool bwd_geometry(int H, int P, bool do_dx, bool do_dw, bool rope, BwdParams* p,
   p->ex_bytes = ((uint32_t)H * 128u + 127u) / 128u * 128u;
   const size_t fixed = 1024 + (do_dx ? (size_t)p->nkb * 8192u : 0) + (prep ? 32768 : 0) +
                        (do_dx ? 16u * p->out_bytes : 0) + (exch ? 16u * p->ex_bytes : 0) +
-                       (prep ? 512 : 0) + 512;  // last: barriers (<= 2*4 + 25 slots)
+                       (prep ? 1024 : 0) + 512;  // last: barriers (<= 2*4 + 25 slots)
   const size_t limit = 227 * 1024;
   p->ns = 4;
   while (p->ns > 2 && fixed + (size_t)p->ns * p->stage_bytes > limit) --p->ns;
