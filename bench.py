@@ -4,7 +4,7 @@
 One step = one pass of every hot-path operation over one batch of seeded
 synthetic inputs, each at its workload's shape:
   premix     LLaMA-2.4B layer shape B=1, N=8192, H=20, P=4, d=128: forward
-             for Q and K (fused RoPE, base 10000) and V; backward (input
+             for Q and K (fused RoPE, base 10000) and V in one launch; backward (input
              gradient, inverse RoPE for Q and K, and weight gradient from the
              same pass over dY) for Q, K, V;
   attention  80 pseudo-heads, N=4096, d=128, causal window W=1024, fp32 LSE,
@@ -12,7 +12,7 @@ synthetic inputs, each at its workload's shape:
   Hiera      MAE stage 1, B=128, 56x56 tokens, 8x8 units, 20 kept, C=d=96:
              gather, attention inside each unit, scatter;
   long ctx   the long-context IHA layer forward, B=2, N=16384, H=20, P=4,
-             d=128: premix Q and K with RoPE and V, then causal attention over
+             d=128: premix Q and K with RoPE and V (one launch), then causal attention over
              the 80 pseudo-heads on those premix outputs (fp32 LSE).
 The step's working set (~5 GB) is far larger than L2 (129 MB), so no L2
 flush is needed between steps: every op's inputs were evicted by the others.
@@ -84,8 +84,7 @@ def op_table():
     tok = pm.B * pm.N
     x_b, y_b, w_b = tok * pm.H * pm.d * 2, tok * pm.HP * pm.d * 2, pm.HP * pm.H * 4
     pf = 2 * tok * pm.HP * pm.H * pm.d
-    for t in "qkv":
-        ops.append((f"premix_fwd_{t}", x_b + y_b + w_b, pf))
+    ops.append(("premix_fwd_qkv", 3 * (x_b + y_b + w_b), 3 * pf))
     for t in "qkv":   # dX and dW from one read of dY and X
         ops.append((f"premix_bwd_{t}", y_b + 2 * x_b + 2 * w_b, 2 * pf))
     aw = S.LLAMA_WINDOW
@@ -104,18 +103,17 @@ def op_table():
     tok = lc.B * lc.N
     x_b, y_b = tok * lc.H * lc.d * 2, tok * lc.HP * lc.d * 2
     pf = 2 * tok * lc.HP * lc.H * lc.d
-    for t in "qkv":
-        ops.append((f"long_premix_fwd_{t}", x_b + y_b + w_b, pf))
+    ops.append(("long_premix_fwd_qkv", 3 * (x_b + y_b + w_b), 3 * pf))
     ops.append(("long_attention_causal", 4 * y_b + lc.B * lc.HP * lc.N * 4,
                 4 * lc.d * _attn_pairs(lc.N, "causal") * lc.HP * lc.B))
     return ops
 
 
 def launches_per_step() -> int:
-    # premix fwd 3; premix bwd 3 x (zero dW + kernel); window attention;
-    # its backward (preprocess, kernel, postprocess); gather, MU attention,
-    # scatter; long-context premix 3 + attention
-    return 3 + 3 * 2 + 1 + 3 + 3 + 3 + 1
+    # premix fwd (Q, K, V in one launch); premix bwd 3 x (zero dW + kernel);
+    # window attention; its backward (preprocess, kernel, postprocess);
+    # gather, MU attention, scatter; long-context premix (one launch) + attention
+    return 1 + 3 * 2 + 1 + 3 + 3 + 1 + 1
 
 
 def _input_recipes(seed: int):
@@ -142,14 +140,14 @@ def host_inputs(seed: int, keys=None):
 
 # inputs each op of the step reads (directly or through the op that feeds it)
 OP_INPUTS = {
-    **{f"premix_fwd_{t}": [f"x_{t}", f"w_{t}"] for t in "qkv"},
+    "premix_fwd_qkv": [f"{a}_{t}" for t in "qkv" for a in "xw"],
     **{f"premix_bwd_{t}": [f"dy_{t}", f"x_{t}", f"w_{t}"] for t in "qkv"},
     "attention_window": ["a_q", "a_k", "a_v"],
     "attention_window_bwd": ["a_q", "a_k", "a_v", "a_do"],
     "mu_gather": ["mu_x", "mu_keep"],
     "mu_attention": ["mu_x", "mu_keep"],
     "mu_scatter": ["mu_x", "mu_keep"],
-    **{f"long_premix_fwd_{t}": [f"lx_{t}", f"lw_{t}"] for t in "qkv"},
+    "long_premix_fwd_qkv": [f"l{a}_{t}" for t in "qkv" for a in "xw"],
     "long_attention_causal": [f"l{a}_{t}" for t in "qkv" for a in "xw"],
 }
 
@@ -217,10 +215,9 @@ class Step:
             k += 1
             mark(k)
 
-        for t in "qkv":
-            T.premix_fwd(i[f"x_{t}"], i[f"w_{t}"], pm.P, rope=(t != "v"), rope_base=S.ROPE_BASE,
-                         out=self.y[t])
-            done()
+        T.premix_fwd_qkv([i[f"x_{t}"] for t in "qkv"], [i[f"w_{t}"] for t in "qkv"], pm.P,
+                         rope=True, rope_base=S.ROPE_BASE, out=tuple(self.y[t] for t in "qkv"))
+        done()
         for t in "qkv":
             T.premix_bwd(i[f"dy_{t}"], i[f"x_{t}"], i[f"w_{t}"], rope=(t != "v"),
                          rope_base=S.ROPE_BASE, dx=self.dx[t], dw=self.dw[t])
@@ -239,10 +236,9 @@ class Step:
         done()
         T.mu_scatter(self.ou, i["mu_keep"], self.dec, mu.grid_h, mu.grid_w, mu.mu_h, mu.mu_w)
         done()
-        for t in "qkv":
-            T.premix_fwd(i[f"lx_{t}"], i[f"lw_{t}"], lc.P, rope=(t != "v"),
-                         rope_base=S.ROPE_BASE, out=self.ly[t])
-            done()
+        T.premix_fwd_qkv([i[f"lx_{t}"] for t in "qkv"], [i[f"lw_{t}"] for t in "qkv"], lc.P,
+                         rope=True, rope_base=S.ROPE_BASE, out=tuple(self.ly[t] for t in "qkv"))
+        done()
         T.mha_fwd(self.ly["q"], self.ly["k"], self.ly["v"], mask=T.MASK_CAUSAL, out=self.lo,
                   lse=self.llse)
         done()
@@ -587,10 +583,16 @@ def single_op(T, torch, name, dev, device):
     e = lambda shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device=device)
     i = dev
     kind, t = name.rsplit("_", 1) if name[-2:] in ("_q", "_k", "_v") else (name, None)
-    if kind == "premix_fwd":
-        y = e((pm.B, pm.N, pm.HP, pm.d))
-        return lambda: T.premix_fwd(i[f"x_{t}"], i[f"w_{t}"], pm.P, rope=(t != "v"),
-                                    rope_base=S.ROPE_BASE, out=y)
+    ly = {u: e((lc.B, lc.N, lc.HP, lc.d)) for u in "qkv"} if kind.startswith("long") else None
+    long_premix = (lambda: T.premix_fwd_qkv([i[f"lx_{u}"] for u in "qkv"],
+                                            [i[f"lw_{u}"] for u in "qkv"], lc.P, rope=True,
+                                            rope_base=S.ROPE_BASE,
+                                            out=tuple(ly[u] for u in "qkv"))
+                   if ly is not None else None)
+    if kind == "premix_fwd_qkv":
+        y = tuple(e((pm.B, pm.N, pm.HP, pm.d)) for _ in range(3))
+        return lambda: T.premix_fwd_qkv([i[f"x_{u}"] for u in "qkv"], [i[f"w_{u}"] for u in "qkv"],
+                                        pm.P, rope=True, rope_base=S.ROPE_BASE, out=y)
     if kind == "premix_bwd":
         dx, dw = e((pm.B, pm.N, pm.H, pm.d)), e((pm.H, pm.P, pm.H), torch.float32)
         return lambda: T.premix_bwd(i[f"dy_{t}"], i[f"x_{t}"], i[f"w_{t}"], rope=(t != "v"),
@@ -624,15 +626,10 @@ def single_op(T, torch, name, dev, device):
             return attn
         attn()
         return scatter
-    if kind == "long_premix_fwd":
-        ly = e((lc.B, lc.N, lc.HP, lc.d))
-        return lambda: T.premix_fwd(i[f"lx_{t}"], i[f"lw_{t}"], lc.P, rope=(t != "v"),
-                                    rope_base=S.ROPE_BASE, out=ly)
+    if kind == "long_premix_fwd_qkv":
+        return long_premix
     if kind == "long_attention_causal":
-        ly = {u: e((lc.B, lc.N, lc.HP, lc.d)) for u in "qkv"}
-        for u in "qkv":
-            T.premix_fwd(i[f"lx_{u}"], i[f"lw_{u}"], lc.P, rope=(u != "v"),
-                         rope_base=S.ROPE_BASE, out=ly[u])
+        long_premix()
         lo, llse = e((lc.B, lc.N, lc.HP, lc.d)), e((lc.B, 1, lc.HP, lc.N), torch.float32)
         return lambda: T.mha_fwd(ly["q"], ly["k"], ly["v"], mask=T.MASK_CAUSAL, out=lo, lse=llse)
     raise ValueError(f"unknown op {name}")

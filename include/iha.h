@@ -88,6 +88,21 @@ iha_status iha_premix_fwd(const void* x, const float* w, void* y, int B, int N,
                           float rope_base, void* stream);
 
 /*
+ * Premix forward of Q, K and V in one launch ("Pseudo-Token Mixing": one
+ * premix per Q, K and V, each with its own weight; the pages fuse the
+ * backward's six launches into two, and this fuses the forward's three into
+ * one).  Tensor t in (q, k, v) computes exactly what iha_premix_fwd computes
+ * for (x_t, w_t, y_t); RoPE (when rope != 0) is applied to q and k only.
+ * All nine buffers follow iha_premix_fwd's layout and limits; no output may
+ * overlap any input or another output.  Shapes outside the tensor-core
+ * kernel run as three launches of the CUDA-core kernel on the same stream.
+ */
+iha_status iha_premix_fwd_qkv(const void* xq, const void* xk, const void* xv,
+                              const float* wq, const float* wk, const float* wv,
+                              void* yq, void* yk, void* yv, int B, int N, int H, int P,
+                              int d, iha_dtype dt, int rope, float rope_base, void* stream);
+
+/*
  * Premix input gradient ("Pseudo-Token Mixing", backward, dX = W^T dY):
  *   dx[b,n,s,f] = sum_{h,p} w[h,p,s] * g[b,n,h*P+p,f]
  * with g = dy, or g = R_n^T dy (inverse rotation) when rope != 0.

@@ -96,6 +96,55 @@ def test_premix_bf16_tensor_core_edges(T, shape, rope):
     _check_all_ops(T, shape, rope, seed=3 + shape[2] * shape[3])
 
 
+def _check_qkv_fwd(T, shape, rope, seed, dtype="bf16", base=100.0):
+    """Q, K, V in one launch: every tensor against the oracle (RoPE on Q and K
+    only), and bit-equal to its own single-tensor launch."""
+    B, N, H, P, d = shape
+    xs = [S.normal((B, N, H, d), seed, 10 + t, dtype=dtype) for t in range(3)]
+    ws = [S.premix_weight(H, P, seed, 20 + t) for t in range(3)]
+    ys = T.premix_fwd_qkv([to_dev(x) for x in xs], [to_dev(w) for w in ws], P, rope=rope,
+                          rope_base=base)
+    for t, (x, w, y) in enumerate(zip(xs, ws, ys)):
+        r = O.premix_fwd(x, w, P, rope=rope and t < 2, rope_base=base)
+        if dtype == "bf16":
+            assert_bf16_close(to_f64(y), r, f"qkv fwd tensor {t}")
+        else:
+            assert_f32_close(to_f64(y), r, f"qkv fwd tensor {t}")
+        one = T.premix_fwd(to_dev(x), to_dev(w), P, rope=rope and t < 2, rope_base=base)
+        assert bool((one.view(-1) == y.view(-1)).all()), f"tensor {t}: differs from its own launch"
+    assert T.device_error() == 0
+
+
+@pytest.mark.parametrize("shape", SHAPES[:3] + TC_EDGE_SHAPES)
+@pytest.mark.parametrize("rope", [False, True])
+def test_premix_qkv_fwd_one_launch(T, shape, rope):
+    if rope and not _rope_ok(shape[4]):
+        pytest.skip("RoPE needs d a power of two")
+    _check_qkv_fwd(T, shape, rope, seed=5 + shape[1])
+
+
+def test_premix_qkv_fwd_f32_tiny_layer(T):
+    sh = S.TINY
+    _check_qkv_fwd(T, (sh.B, sh.N, sh.H, sh.P, sh.d), True, seed=9, dtype="f32")
+
+
+def test_premix_qkv_fwd_llama_shape_sampled(T):
+    """B=1, N=8192, H=20, P=4, d=128 in one launch: sampled token windows of
+    each tensor against the oracle (positions enter through RoPE)."""
+    import torch
+    B, N, H, P, d = 1, 8192, 20, 4, 128
+    xs = [S.normal((B, N, H, d), 31, t) for t in range(3)]
+    ws = [S.premix_weight(H, P, 31, 10 + t) for t in range(3)]
+    ys = T.premix_fwd_qkv([to_dev(x) for x in xs], [to_dev(w) for w in ws], P, rope=True)
+    torch.cuda.synchronize()
+    for n0 in (0, 4093, N - 64):
+        for t in range(3):
+            r = O.premix_fwd(np.ascontiguousarray(xs[t][:, n0:n0 + 64]), ws[t], P, rope=t < 2,
+                             pos0=n0)
+            assert_bf16_close(to_f64(ys[t][:, n0:n0 + 64]), r, f"qkv llama tensor {t} @{n0}")
+    assert T.device_error() == 0
+
+
 @pytest.mark.parametrize("rope", [False, True])
 def test_premix_f32_tiny_layer(T, rope):
     """fp32 path at the tiny-layer shape (B=1, N=128, H=4, P=2, d=32): 1e-5."""

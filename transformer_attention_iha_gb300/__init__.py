@@ -33,7 +33,7 @@ MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW = 0, 1, 2
 SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",
            "mha_fwd", "mu_gather", "mu_scatter", "iha_status_string", "iha_last_error",
            "iha_device_error", "iha_test_fail_next_wait", "mha_bwd", "mha_bwd_workspace_bytes",
-           "mha_bwd_noalloc")
+           "mha_bwd_noalloc", "iha_premix_fwd_qkv")
 
 
 class IHAError(RuntimeError):
@@ -66,6 +66,7 @@ def lib() -> C.CDLL:
     L = C.CDLL(_build.LIB)
     vp, i, f = C.c_void_p, C.c_int, C.c_float
     L.iha_premix_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    L.iha_premix_fwd_qkv.argtypes = [vp] * 9 + [i, i, i, i, i, i, i, f, vp]
     L.iha_premix_bwd_dx.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.iha_premix_bwd_dw.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.iha_premix_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
@@ -79,8 +80,9 @@ def lib() -> C.CDLL:
     L.mha_bwd_noalloc.restype = C.c_int
     L.mu_gather.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     L.mu_scatter.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
-    for name in ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",
-                 "mha_fwd", "mha_bwd", "mu_gather", "mu_scatter"):
+    for name in ("iha_premix_fwd", "iha_premix_fwd_qkv", "iha_premix_bwd_dx",
+                 "iha_premix_bwd_dw", "iha_premix_bwd", "mha_fwd", "mha_bwd", "mu_gather",
+                 "mu_scatter"):
         getattr(L, name).restype = C.c_int
     L.iha_status_string.argtypes = [i]
     L.iha_status_string.restype = C.c_char_p
@@ -168,6 +170,34 @@ def premix_fwd(x, w, P: int, rope: bool = False, rope_base: float = 10000.0, out
     check(lib().iha_premix_fwd(_ptr(x), _ptr(w), _ptr(out), B, N, H, P, d, _dt(x), int(rope),
                                float(rope_base), _stream(stream)), "iha_premix_fwd")
     return out
+
+
+def premix_fwd_qkv(xs, ws, P: int, rope: bool = False, rope_base: float = 10000.0, out=None,
+                   stream=None):
+    """(Y_q, Y_k, Y_v) = premix of (X_q, X_k, X_v) with (W_q, W_k, W_v) in one
+    launch; RoPE (when rope) on Q and K only."""
+    torch = _torch()
+    if len(xs) != 3 or len(ws) != 3:
+        raise ValueError("xs and ws must hold three tensors (q, k, v)")
+    x0 = xs[0]
+    _expect(x0, "xq")
+    if x0.dim() != 4:
+        raise ValueError("x must be [B, N, H, d]")
+    B, N, H, d = x0.shape
+    for t, (x, w) in enumerate(zip(xs, ws)):
+        _expect(x, f"x[{t}]", (B, N, H, d), x0.dtype, x0.device)
+        _expect(w, f"w[{t}]", (H, P, H), torch.float32, x0.device)
+    if out is None:
+        out = tuple(torch.empty((B, N, H * P, d), dtype=x0.dtype, device=x0.device)
+                    for _ in range(3))
+    if len(out) != 3:
+        raise ValueError("out must hold three tensors")
+    for t, y in enumerate(out):
+        _expect(y, f"out[{t}]", (B, N, H * P, d), x0.dtype, x0.device)
+    check(lib().iha_premix_fwd_qkv(*(_ptr(x) for x in xs), *(_ptr(w) for w in ws),
+                                   *(_ptr(y) for y in out), B, N, H, P, d, _dt(x0), int(rope),
+                                   float(rope_base), _stream(stream)), "iha_premix_fwd_qkv")
+    return tuple(out)
 
 
 def premix_bwd_dx(dy, w, rope: bool = False, rope_base: float = 10000.0, out=None,

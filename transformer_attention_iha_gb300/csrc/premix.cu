@@ -591,6 +591,40 @@ iha_status iha_premix_fwd(const void* x, const float* w, void* y, int B, int N, 
   return check_launch("iha_premix_fwd");
 }
 
+iha_status iha_premix_fwd_qkv(const void* xq, const void* xk, const void* xv, const float* wq,
+                              const float* wk, const float* wv, void* yq, void* yk, void* yv,
+                              int B, int N, int H, int P, int d, iha_dtype dt, int rope,
+                              float rope_base, void* stream) {
+  using namespace iha;
+  const void* x[3] = {xq, xk, xv};
+  const float* w[3] = {wq, wk, wv};
+  void* y[3] = {yq, yk, yv};
+  for (int t = 0; t < 3; ++t) {
+    iha_status st = check_common("iha_premix_fwd_qkv", x[t], w[t], y[t], B, N, H, P, d, dt,
+                                 t < 2 ? rope : 0, rope_base);
+    if (st != IHA_OK) return st;
+  }
+  const PremixGeom g = make_geom(B, N, H, P, d, rope_base);
+  const size_t es = dt == IHA_BF16 ? 2 : 4;
+  const size_t ny = g.ntok * g.HP * d * es, nx = g.ntok * H * d * es, nw = (size_t)g.HP * H * 4;
+  for (int t = 0; t < 3; ++t)
+    for (int u = 0; u < 3; ++u)
+      if (overlaps(y[t], ny, x[u], nx) || overlaps(y[t], ny, w[u], nw) ||
+          (u != t && overlaps(y[t], ny, y[u], ny)))
+        return fail(IHA_ERR_INVALID_ARG, "iha_premix_fwd_qkv: an output overlaps another tensor");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == IHA_BF16 && premix_tc_supported(H, P, d))
+    return premix_fwd_tc_multi(3, x, w, y, B, N, H, P, d, rope ? 3 : 0, rope_base, s);
+  for (int t = 0; t < 3; ++t) {
+    const bool r = t < 2 && rope;
+    if (dt == IHA_BF16) launch_fwd<__nv_bfloat16>(g, x[t], w[t], y[t], r, s);
+    else launch_fwd<float>(g, x[t], w[t], y[t], r, s);
+    const iha_status st = check_launch("iha_premix_fwd_qkv");
+    if (st != IHA_OK) return st;
+  }
+  return IHA_OK;
+}
+
 iha_status iha_premix_bwd_dx(const void* dy, const float* w, void* dx, int B, int N, int H,
                              int P, int d, iha_dtype dt, int rope, float rope_base,
                              void* stream) {

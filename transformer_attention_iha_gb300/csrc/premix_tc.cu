@@ -13,6 +13,11 @@
 // mix to far below the bf16 output rounding.  At H = 20 this moves the 2*H
 // flops per output off the fp32 pipe, which alone could not keep up with HBM.
 //
+// One launch can mix up to three tensors (Q, K, V: each its own X, W, Y and
+// RoPE flag).  The CTA walks stages of the concatenated token-pair lists;
+// the three bf16 hi | lo weight tiles sit side by side in shared memory,
+// spaced by the rows they use (ceil(H*P / 8) groups of 8 rows), since the
+// MMA rows beyond H*P only feed accumulator rows that are never stored.
 // Roles (320 threads, one CTA per SM, persistent over token pairs):
 //   warps 0-7  epilogue: warp e reads TMEM lanes 32*(e%4).. (pseudo-head rows)
 //              of token e/4 of the pair: 128 fp32 columns per thread, RoPE in
@@ -40,10 +45,20 @@ constexpr int kEpiThreads = 256;
 constexpr int kXStages = 4;
 constexpr int kTok = 2;  // tokens per stage
 
+constexpr int kMaxTens = 3;
+
 struct FwdParams {
-  int ntok, N, H, HP, d, nch, rope, n_stages;
-  uint32_t stage_bytes;  // X bytes per stage
+  int ntok, N, H, HP, d, nch, n_stages;  // n_stages: token pairs per tensor
+  int ntens, rope_mask;                  // tensors of the launch; bit t: RoPE on tensor t
+  int x_stages;                          // depth of the X ring (<= kXStages)
+  uint32_t stage_bytes;                  // X bytes per stage
+  uint32_t w_spacing;                    // bytes between the weight tiles
+  const float* w[kMaxTens];
   RopeTable rt;
+};
+
+struct FwdMaps {
+  CUtensorMap x[kMaxTens], y[kMaxTens];
 };
 
 // cos / sin of n * inv_freq with inv_freq = hi + lo (fp32 pair).  The product
@@ -80,17 +95,15 @@ __device__ __forceinline__ void raise_error(volatile int* abort_flag) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    premix_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX,
-                         const __grid_constant__ CUtensorMap tmY, const float* __restrict__ w,
-                         const FwdParams p) {
+    premix_fwd_tc_kernel(const __grid_constant__ FwdMaps maps, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr int NCH = D / 64, HALF = D / 2;
   constexpr uint32_t kWarpStage = 2u * NCH * 4096u;  // per epilogue warp: 2 buffers x NCH x [32][64]
-  const uint32_t sW = smem_u32(smem);                      // 16 KB
-  const uint32_t sX = sW + 16384;                          // kXStages x stage_bytes
-  const uint32_t sStage = sX + kXStages * p.stage_bytes;   // 8 warps x kWarpStage
+  const uint32_t sW = smem_u32(smem);                      // weight tiles
+  const uint32_t sX = sW + (uint32_t)(p.ntens - 1) * p.w_spacing + 16384u;  // X ring
+  const uint32_t sStage = sX + (uint32_t)p.x_stages * p.stage_bytes;  // 8 warps x kWarpStage
   // per epilogue warp: cos / sin of its token, [HALF / 2] x (c_2j, c_2j+1, s_2j, s_2j+1)
   float4* rope_tabs = reinterpret_cast<float4*>(smem + (sStage - sW) + 8 * kWarpStage);  // [8][32]
   float2* inv_tab = reinterpret_cast<float2*>(rope_tabs + 8 * 32);  // [64] inv_freq (hi, lo)
@@ -102,12 +115,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto b_accempty = [&](int a) { return bar0 + 8u * (2 * kXStages + 2 + a); };
   const uint32_t b_drain = bar0 + 8u * (2 * kXStages + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kXStages + 5);
+  const int XS = p.x_stages;
+  const int total_stages = p.ntens * p.n_stages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kXStages; ++s) {
+    for (int s = 0; s < XS; ++s) {
       mbar_init(b_xfull(s), 1);
       mbar_init(b_xempty(s), 1);
     }
@@ -121,10 +136,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < 64; ++i) inv_tab[i] = make_float2(p.rt.hi[i], p.rt.lo[i]);
   }
-  // W -> bf16 hi | lo, K-major rows of 64 (hi s0..31 | lo s0..31), 128B swizzle
+  // W -> bf16 hi | lo, K-major rows of 64 (hi s0..31 | lo s0..31), 128B swizzle,
+  // one tile per tensor; only rows < H*P are written (the next tile starts
+  // there).  Rows of the last tile past H*P stay unwritten: they only reach
+  // accumulator rows that are never read.
   if (tid < kEpiThreads) {
-    for (int idx = tid; idx < 128 * 8; idx += kEpiThreads) {
-      const int row = idx >> 3, j = idx & 7;
+    const int rows8 = (p.HP + 7) & ~7;
+    for (int idx = tid; idx < p.ntens * rows8 * 8; idx += kEpiThreads) {
+      const int tns = idx / (rows8 * 8), r = idx - tns * rows8 * 8;
+      const int row = r >> 3, j = r & 7;
+      const float* w = p.w[0];
+      if (tns == 1) w = p.w[1];
+      if (tns == 2) w = p.w[2];
       uint32_t v[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -139,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         v[e] = pack_bf16x2(part[0], part[1]);
       }
-      const uint32_t off = (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((j ^ (row & 7)) << 4));
+      const uint32_t off = (uint32_t)tns * p.w_spacing +
+                           (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((j ^ (row & 7)) << 4));
       *reinterpret_cast<uint4*>(smem + off) = make_uint4(v[0], v[1], v[2], v[3]);
     }
     fence_proxy_async_smem();
@@ -156,22 +180,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmX);
+      for (int t = 0; t < p.ntens; ++t) tma_prefetch_desc(&maps.x[t]);
       int k = 0;
-      for (int g = blockIdx.x; g < p.n_stages; g += gridDim.x, ++k) {
-        const int xs = k % kXStages;
-        if (!mbar_wait(b_xempty(xs), ((k / kXStages) & 1) ^ 1, abort_flag)) {
+      for (int G = blockIdx.x; G < total_stages; G += gridDim.x, ++k) {
+        const int tns = G / p.n_stages, g = G - tns * p.n_stages;
+        const int xs = k % XS;
+        if (!mbar_wait(b_xempty(xs), ((k / XS) & 1) ^ 1, abort_flag)) {
           raise_error(abort_flag);
           break;
         }
         mbar_arrive_expect_tx(b_xfull(xs), p.stage_bytes);
-        tma_load_4d(sX + xs * p.stage_bytes, &tmX, b_xfull(xs), 0, 0, 0, g * kTok);
+        tma_load_4d(sX + xs * p.stage_bytes, &maps.x[tns], b_xfull(xs), 0, 0, 0, g * kTok);
       }
       // Whoever aborted, no copy may still be landing when the CTA exits
       // (in a normal run the last loads have completed and this returns at once).
       volatile int no_abort = 0;
-      for (int kk = k - kXStages > 0 ? k - kXStages : 0; kk < k; ++kk)
-        mbar_wait(b_xfull(kk % kXStages), (kk / kXStages) & 1, &no_abort);
+      for (int kk = k - XS > 0 ? k - XS : 0; kk < k; ++kk)
+        mbar_wait(b_xfull(kk % XS), (kk / XS) & 1, &no_abort);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -180,9 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nks = (p.H + 15) >> 4;
       int k = 0;
       bool ok = true;
-      for (int g = blockIdx.x; g < p.n_stages; g += gridDim.x, ++k) {
-        const int xs = k % kXStages, a = k & 1;
-        if (!(ok = mbar_wait(b_xfull(xs), (k / kXStages) & 1, abort_flag))) break;
+      for (int G = blockIdx.x; G < total_stages; G += gridDim.x, ++k) {
+        const int tns = G / p.n_stages;
+        const uint32_t wt = sW + (uint32_t)tns * p.w_spacing;
+        const int xs = k % XS, a = k & 1;
+        if (!(ok = mbar_wait(b_xfull(xs), (k / XS) & 1, abort_flag))) break;
         if (!(ok = mbar_wait(b_accempty(a), ((k >> 1) & 1) ^ 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(a * 256);
@@ -190,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int j = 0;
         for (int part = 0; part < 2; ++part)
           for (int ks = 0; ks < nks; ++ks, ++j)
-            mma_ss(d_tmem, smem_desc_sw128(sW + part * 64 + ks * 32, 16, 1024),
+            mma_ss(d_tmem, smem_desc_sw128(wt + part * 64 + ks * 32, 16, 1024),
                    smem_desc_sw128(xbase + ks * 2048, 32 * 128, 1024), idesc, j > 0 ? 1u : 0u);
         mma_commit(b_xempty(xs));
         mma_commit(b_accfull(a));
@@ -210,10 +237,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t wstage = sStage + (uint32_t)warp * kWarpStage;
     float4* tab = rope_tabs + warp * 32;
     int k = 0;
-    for (int g = blockIdx.x; g < p.n_stages; g += gridDim.x, ++k) {
+    for (int G = blockIdx.x; G < total_stages; G += gridDim.x, ++k) {
+      const int tns = G / p.n_stages, g = G - tns * p.n_stages;
+      const bool rope = (p.rope_mask >> tns) & 1;
       const int a = k & 1, sb = k & 1;
       const int t = g * kTok + tt;
-      if (p.rope && warp_active && 2 * lane < HALF) {
+      if (rope && warp_active && 2 * lane < HALF) {
         float c0, s0, c1, s1;
         const float4 inv = reinterpret_cast<const float4*>(inv_tab)[lane];  // pairs 2 lane, 2 lane + 1
         rope_cos_sin(t % p.N, inv.x, inv.y, c0, s0);
@@ -246,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(b_accempty(a));
         }
         if (work && row < p.HP) {
-          if (p.rope) {
+          if (rope) {
             // pairs (i, i + HALF) two at a time on the packed fp32 pipe
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -287,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
 #pragma unroll
           for (int c = 0; c < NCH; ++c)
-            tma_store_3d(&tmY, wstage + (uint32_t)(sb * NCH + c) * 4096u, 64 * c, q * 32, t);
+            tma_store_3d(&maps.y[tns], wstage + (uint32_t)(sb * NCH + c) * 4096u, 64 * c, q * 32, t);
           bulk_commit();
         }
       }
@@ -322,8 +351,9 @@ void make_rope_table(RopeTable* rt, int d, float base) {
   }
 }
 
-iha_status premix_fwd_tc(const void* x, const float* w, void* y, int B, int N, int H, int P,
-                         int d, int rope, float rope_base, cudaStream_t stream) {
+iha_status premix_fwd_tc_multi(int ntens, const void* const* x, const float* const* w,
+                               void* const* y, int B, int N, int H, int P, int d, int rope_mask,
+                               float rope_base, cudaStream_t stream) {
   FwdParams p;
   p.ntok = B * N;
   p.N = N;
@@ -331,39 +361,59 @@ iha_status premix_fwd_tc(const void* x, const float* w, void* y, int B, int N, i
   p.HP = H * P;
   p.d = d;
   p.nch = d / 64;
-  p.rope = rope;
+  p.ntens = ntens;
+  p.rope_mask = rope_mask;
   p.n_stages = (p.ntok + kTok - 1) / kTok;
   p.stage_bytes = (uint32_t)(kTok * p.nch * 32 * 128);
+  p.w_spacing = (uint32_t)((p.HP + 7) / 8) * 1024u;
+  for (int t = 0; t < kMaxTens; ++t) p.w[t] = w[t < ntens ? t : 0];
   make_rope_table(&p.rt, d, rope_base);
 
-  CUtensorMap mx, my;
-  {
-    // X as [tokens][d/64][s][64]: box = 64 features x 32 heads x d/64 x 2 tokens
-    uint64_t dims[4] = {64, (uint64_t)H, (uint64_t)p.nch, (uint64_t)p.ntok};
-    uint64_t st[3] = {(uint64_t)d * 2, 128, (uint64_t)H * d * 2};
-    uint32_t box[4] = {64, 32, (uint32_t)p.nch, (uint32_t)kTok};
-    if (encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, st, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return fail(IHA_ERR_CUDA, "iha_premix_fwd: X tensor map encoding failed");
+  FwdMaps maps;
+  for (int t = 0; t < kMaxTens; ++t) {
+    const int u = t < ntens ? t : 0;
+    {
+      // X as [tokens][d/64][s][64]: box = 64 features x 32 heads x d/64 x 2 tokens
+      uint64_t dims[4] = {64, (uint64_t)H, (uint64_t)p.nch, (uint64_t)p.ntok};
+      uint64_t st[3] = {(uint64_t)d * 2, 128, (uint64_t)H * d * 2};
+      uint32_t box[4] = {64, 32, (uint32_t)p.nch, (uint32_t)kTok};
+      if (encode_tiled(&maps.x[t], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x[u]),
+                       dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return fail(IHA_ERR_CUDA, "premix forward: X tensor map encoding failed");
+    }
+    {
+      uint64_t dims[3] = {(uint64_t)d, (uint64_t)p.HP, (uint64_t)p.ntok};
+      uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)p.HP * d * 2};
+      uint32_t box[3] = {64, 32, 1};
+      if (encode_tiled(&maps.y[t], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y[u], dims, st, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return fail(IHA_ERR_CUDA, "premix forward: Y tensor map encoding failed");
+    }
   }
-  {
-    uint64_t dims[3] = {(uint64_t)d, (uint64_t)p.HP, (uint64_t)p.ntok};
-    uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)p.HP * d * 2};
-    uint32_t box[3] = {64, 32, 1};
-    if (encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, dims, st, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return fail(IHA_ERR_CUDA, "iha_premix_fwd: Y tensor map encoding failed");
-  }
-  const size_t smem = 1024 + 16384 + kXStages * p.stage_bytes + 8 * 2 * p.nch * 4096 +
-                      8 * 32 * sizeof(float4) + 64 * sizeof(float2) + 256;
+  // shared memory: alignment slack | weight tiles | X ring | epilogue staging |
+  // cos / sin tables | inv_freq table | barriers; the ring is 4 deep when it fits
+  const size_t fixed = 1024 + (size_t)(ntens - 1) * p.w_spacing + 16384 +
+                       8 * 2 * p.nch * 4096 + 8 * 32 * sizeof(float4) + 64 * sizeof(float2) + 256;
+  p.x_stages = kXStages;
+  while (p.x_stages > 2 && fixed + (size_t)p.x_stages * p.stage_bytes > 227 * 1024) --p.x_stages;
+  const size_t smem = fixed + (size_t)p.x_stages * p.stage_bytes;
+  if (smem > 227 * 1024) return fail(IHA_ERR_UNSUPPORTED, "premix forward: shared memory budget");
   auto kern = d == 128 ? premix_fwd_tc_kernel<128> : premix_fwd_tc_kernel<64>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
-    return check_launch("iha_premix_fwd (smem attribute)");
+    return check_launch("premix forward (smem attribute)");
   int grid = sm_count();
-  if (grid > p.n_stages) grid = p.n_stages;
-  kern<<<grid, kThreads, smem, stream>>>(mx, my, w, p);
-  return check_launch("iha_premix_fwd");
+  if (grid > ntens * p.n_stages) grid = ntens * p.n_stages;
+  kern<<<grid, kThreads, smem, stream>>>(maps, p);
+  return check_launch("premix forward");
+}
+
+iha_status premix_fwd_tc(const void* x, const float* w, void* y, int B, int N, int H, int P,
+                         int d, int rope, float rope_base, cudaStream_t stream) {
+  const void* xs[1] = {x};
+  const float* ws[1] = {w};
+  void* ys[1] = {y};
+  return premix_fwd_tc_multi(1, xs, ws, ys, B, N, H, P, d, rope ? 1 : 0, rope_base, stream);
 }
 
 }  // namespace iha

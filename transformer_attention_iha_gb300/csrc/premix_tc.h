@@ -33,4 +33,10 @@ iha_status premix_bwd_tc(const void* dy, const void* x, const float* w, void* dx
 iha_status premix_fwd_tc(const void* x, const float* w, void* y, int B, int N, int H, int P,
                          int d, int rope, float rope_base, cudaStream_t stream);
 
+// The same forward over ntens (1..3) tensors in one launch; tensor t reads
+// x[t], w[t], writes y[t], and is rotated when bit t of rope_mask is set.
+iha_status premix_fwd_tc_multi(int ntens, const void* const* x, const float* const* w,
+                               void* const* y, int B, int N, int H, int P, int d, int rope_mask,
+                               float rope_base, cudaStream_t stream);
+
 }  // namespace iha
