@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the schedule; one elected lane issues (see elect_one).
+    {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, NCH * kChunk, false, true);
       const uint32_t tS0 = tmem, tS1 = tmem + 128u, tO0 = tmem + 256u, tO1 = tmem + 384u;
@@ -258,18 +259,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       auto issue_qk = [&](uint32_t dS, uint64_t dq, uint32_t kslot) {
         const uint64_t dk = dK0 + kKSlotDesc * kslot;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 4 * NCH; ++kk) {
-          const uint64_t off = (uint64_t)(((kk >> 2) * kTileChunkBytes + (kk & 3) * 32) >> 4);
-          mma_ss_nm(dS, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4 * NCH; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * kTileChunkBytes + (kk & 3) * 32) >> 4);
+            mma_ss_nm(dS, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
+          }
         }
+        __syncwarp();
       };
       auto issue_pv = [&](uint32_t dO, uint32_t aP, uint32_t vslot, uint32_t first) {
         const uint64_t dv = vslot ? dV1 : dV0;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_nm(dO, aP + (uint32_t)(kk * 8), dv + (uint64_t)(kk * 128), idesc_pv,
-                    (kk > 0 || !first) ? 1u : 0u);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts_nm(dO, aP + (uint32_t)(kk * 8), dv + (uint64_t)(kk * 128), idesc_pv,
+                      (kk > 0 || !first) ? 1u : 0u);
+        }
+        __syncwarp();
       };
       for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
         const Item it = decode_item(p, idx);
@@ -279,73 +286,73 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t q = (uint32_t)(j - it.jlo);
           while (ok && k_ready <= q) {
             const uint32_t n = kbase + k_ready;
-            ok = mbar_wait(b_kfull(n % kKSlots), (n / kKSlots) & 1, abort_flag, lim);
+            ok = mbar_wait_warp(b_kfull(n % kKSlots), (n / kKSlots) & 1, abort_flag, lim);
             ++k_ready;
           }
           return ok;
         };
         // prologue: first QK^T of each tile
-        if ((ok = mbar_wait(b_qfull(0), qn0 & 1, abort_flag, lim)) && wait_k(it.lo0)) {
+        if ((ok = mbar_wait_warp(b_qfull(0), qn0 & 1, abort_flag, lim)) && wait_k(it.lo0)) {
           ++qn0;
           tc_fence_after();
           issue_qk(tS0, dQ0, (kbase + (uint32_t)(it.lo0 - it.jlo)) % kKSlots);
-          mma_commit(b_sfull(0));
-          if (it.lo0 == it.hi0) mma_commit(b_qempty(0));
+          mma_commit_warp(b_sfull(0));
+          if (it.lo0 == it.hi0) mma_commit_warp(b_qempty(0));
         }
         if (ok && it.act1) {
-          if ((ok = mbar_wait(b_qfull(1), qn1 & 1, abort_flag, lim)) && wait_k(it.lo1)) {
+          if ((ok = mbar_wait_warp(b_qfull(1), qn1 & 1, abort_flag, lim)) && wait_k(it.lo1)) {
             ++qn1;
             tc_fence_after();
             issue_qk(tS1, dQ1, (kbase + (uint32_t)(it.lo1 - it.jlo)) % kKSlots);
-            mma_commit(b_sfull(1));
-            if (it.lo1 == it.hi1) mma_commit(b_qempty(1));
+            mma_commit_warp(b_sfull(1));
+            if (it.lo1 == it.hi1) mma_commit_warp(b_qempty(1));
           }
         }
         for (int j = it.jlo; ok && j <= it.jhi; ++j) {
           const uint32_t nk = kbase + (uint32_t)(j - it.jlo), nv = vbase + (uint32_t)(j - it.jlo);
           // every QK^T reading K(j) has been issued: release its slot when they finish
-          mma_commit(b_kempty(nk % kKSlots));
-          if (!(ok = mbar_wait(b_vfull(nv & 1), (nv >> 1) & 1, abort_flag, lim))) break;
+          mma_commit_warp(b_kempty(nk % kKSlots));
+          if (!(ok = mbar_wait_warp(b_vfull(nv & 1), (nv >> 1) & 1, abort_flag, lim))) break;
           const uint32_t knext = (nk + 1) % kKSlots;
           // tile 0
           if (j >= it.lo0 && j <= it.hi0) {
-            if (!(ok = mbar_wait(b_pfull(0), pn0 & 1, abort_flag, lim))) break;
+            if (!(ok = mbar_wait_warp(b_pfull(0), pn0 & 1, abort_flag, lim))) break;
             ++pn0;
             tc_fence_after();
             issue_pv(tO0, tS0, nv & 1, j == it.lo0);
             if (j == it.hi0) {
-              mma_commit(b_ofull(0));
+              mma_commit_warp(b_ofull(0));
             } else {
               if (!wait_k(j + 1)) break;
               tc_fence_after();
               issue_qk(tS0, dQ0, knext);
-              mma_commit(b_sfull(0));
-              if (j + 1 == it.hi0) mma_commit(b_qempty(0));  // last use of Q tile 0
+              mma_commit_warp(b_sfull(0));
+              if (j + 1 == it.hi0) mma_commit_warp(b_qempty(0));  // last use of Q tile 0
             }
           }
           // tile 1
           if (it.act1 && j >= it.lo1 && j <= it.hi1) {
-            if (!(ok = mbar_wait(b_pfull(1), pn1 & 1, abort_flag, lim))) break;
+            if (!(ok = mbar_wait_warp(b_pfull(1), pn1 & 1, abort_flag, lim))) break;
             ++pn1;
             tc_fence_after();
             issue_pv(tO1, tS1, nv & 1, j == it.lo1);
             if (j == it.hi1) {
-              mma_commit(b_ofull(1));
+              mma_commit_warp(b_ofull(1));
             } else {
               if (!wait_k(j + 1)) break;
               tc_fence_after();
               issue_qk(tS1, dQ1, knext);
-              mma_commit(b_sfull(1));
-              if (j + 1 == it.hi1) mma_commit(b_qempty(1));
+              mma_commit_warp(b_sfull(1));
+              if (j + 1 == it.hi1) mma_commit_warp(b_qempty(1));
             }
           }
-          mma_commit(b_vempty(nv & 1));
+          mma_commit_warp(b_vempty(nv & 1));
         }
         kc = kbase + (uint32_t)(it.jhi - it.jlo + 1);
         vc = vbase + (uint32_t)(it.jhi - it.jlo + 1);
       }
       if (!ok) raise_error(abort_flag);
-      mma_drain(b_drain);  // no MMA in flight when TMEM is released
+      mma_drain_warp(b_drain);  // no MMA in flight when TMEM is released
     }
   } else {
     // ------------------------------------------------------------ softmax warps
