@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the schedule; one elected lane issues (see elect_one).
+    {
       const uint32_t id_sq = idesc_bf16_f32(128, 128, false, false);      // S^T, dP^T
       const uint32_t id_acc = idesc_bf16_f32(128, p.ksteps * 16, false, true);  // dV, dK
       const uint32_t id_dq = idesc_bf16_f32(128, 128, true, true);        // dQ^T
@@ -228,76 +229,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ni = 0, gt = 0;  // items, query tiles (global count)
       for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++ni) {
         const Item it = decode_item(p, idx);
-        if (!(ok = mbar_wait(b_kvfull, ni & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(b_kvfull, ni & 1, abort_flag))) break;
         // dK / dV of the previous item have been read out
-        if (ni > 0 && !(ok = mbar_wait(b_kvoutempty, (ni - 1) & 1, abort_flag))) break;
+        if (ni > 0 && !(ok = mbar_wait_warp(b_kvoutempty, (ni - 1) & 1, abort_flag))) break;
         for (int qt = it.qlo; ok && qt <= it.qhi; ++qt, ++gt) {
           const int s = gt & 1, r = gt & 1;
           const uint32_t tS = tmem + 128u * r, tP = tmem + 128u * (r ^ 1);
           const uint32_t q_s = sQ + 2 * s * kTileB, do_s = sDO + 2 * s * kTileB;
-          if (!(ok = mbar_wait(b_qfull(s), (gt >> 1) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(b_qfull(s), (gt >> 1) & 1, abort_flag))) break;
           tc_fence_after();
           // S^T = K Q^T  (M = keys, N = queries, K = d)
           {
             const uint64_t da = smem_desc_sw128(sK, 16, 1024), db = smem_desc_sw128(q_s, 16, 1024);
-            for (int kk = 0; kk < p.ksteps; ++kk) {
-              const uint64_t off = (uint64_t)(((kk >> 2) * kChunkB + (kk & 3) * 32) >> 4);
-              mma_ss_nm(tS, da + off, db + off, id_sq, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(b_sfull);
+            if (elect_one())
+              for (int kk = 0; kk < p.ksteps; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * kChunkB + (kk & 3) * 32) >> 4);
+                mma_ss_nm(tS, da + off, db + off, id_sq, kk > 0 ? 1u : 0u);
+              }
+            __syncwarp();
+            mma_commit_warp(b_sfull);
           }
           // dP^T = V dO^T into the region dQ^T of the previous tile used
-          if (gt >= 1 && !(ok = mbar_wait(b_dqempty(r ^ 1), ((gt - 1) >> 1) & 1, abort_flag)))
+          if (gt >= 1 && !(ok = mbar_wait_warp(b_dqempty(r ^ 1), ((gt - 1) >> 1) & 1, abort_flag)))
             break;
           tc_fence_after();
           {
             const uint64_t da = smem_desc_sw128(sV, 16, 1024), db = smem_desc_sw128(do_s, 16, 1024);
-            for (int kk = 0; kk < p.ksteps; ++kk) {
-              const uint64_t off = (uint64_t)(((kk >> 2) * kChunkB + (kk & 3) * 32) >> 4);
-              mma_ss_nm(tP, da + off, db + off, id_sq, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(b_dpfull);
+            if (elect_one())
+              for (int kk = 0; kk < p.ksteps; ++kk) {
+                const uint64_t off = (uint64_t)(((kk >> 2) * kChunkB + (kk & 3) * 32) >> 4);
+                mma_ss_nm(tP, da + off, db + off, id_sq, kk > 0 ? 1u : 0u);
+              }
+            __syncwarp();
+            mma_commit_warp(b_dpfull);
           }
           const bool first = qt == it.qlo;
           // dV += P^T dO  (M = keys, N = d, K = queries)
-          if (!(ok = mbar_wait(b_ptfull, gt & 1, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(b_ptfull, gt & 1, abort_flag))) break;
           tc_fence_after();
           {
             const uint64_t da = smem_desc_sw128(sPS, 16, 1024);
             const uint64_t db = smem_desc_sw128(do_s, kChunkB, 1024);
-            for (int kk = 0; kk < kB / 16; ++kk) {
-              const uint64_t offa = (uint64_t)(((kk >> 2) * kChunkB + (kk & 3) * 32) >> 4);
-              mma_ss_nm(tDV, da + offa, db + (uint64_t)(kk * 128), id_acc,
-                        (!first || kk > 0) ? 1u : 0u);
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < kB / 16; ++kk) {
+                const uint64_t offa = (uint64_t)(((kk >> 2) * kChunkB + (kk & 3) * 32) >> 4);
+                mma_ss_nm(tDV, da + offa, db + (uint64_t)(kk * 128), id_acc,
+                          (!first || kk > 0) ? 1u : 0u);
+              }
             }
-            mma_commit(b_dvdone);
+            __syncwarp();
+            mma_commit_warp(b_dvdone);
           }
           // dK += dS^T Q ;  dQ^T = K^T dS^T (M = features, N = queries, K = keys)
-          if (!(ok = mbar_wait(b_dsfull, gt & 1, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(b_dsfull, gt & 1, abort_flag))) break;
           tc_fence_after();
           {
             const uint64_t da = smem_desc_sw128(sPS, 16, 1024);
             const uint64_t db = smem_desc_sw128(q_s, kChunkB, 1024);
-            for (int kk = 0; kk < kB / 16; ++kk) {
-              const uint64_t offa = (uint64_t)(((kk >> 2) * kChunkB + (kk & 3) * 32) >> 4);
-              mma_ss_nm(tDK, da + offa, db + (uint64_t)(kk * 128), id_acc,
-                        (!first || kk > 0) ? 1u : 0u);
-            }
             const uint64_t dka = smem_desc_sw128(sK, kChunkB, 1024);
             const uint64_t dsb = smem_desc_sw128(sPS, kChunkB, 1024);
-            for (int kk = 0; kk < kB / 16; ++kk)
-              mma_ss_nm(tS, dka + (uint64_t)(kk * 128), dsb + (uint64_t)(kk * 128), id_dq,
-                        kk > 0 ? 1u : 0u);
-            mma_commit(b_dqfull(r));
-            mma_commit(b_psfree);  // dK and dQ^T have read dS^T
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < kB / 16; ++kk) {
+                const uint64_t offa = (uint64_t)(((kk >> 2) * kChunkB + (kk & 3) * 32) >> 4);
+                mma_ss_nm(tDK, da + offa, db + (uint64_t)(kk * 128), id_acc,
+                          (!first || kk > 0) ? 1u : 0u);
+              }
+#pragma unroll
+              for (int kk = 0; kk < kB / 16; ++kk)
+                mma_ss_nm(tS, dka + (uint64_t)(kk * 128), dsb + (uint64_t)(kk * 128), id_dq,
+                          kk > 0 ? 1u : 0u);
+            }
+            __syncwarp();
+            mma_commit_warp(b_dqfull(r));
+            mma_commit_warp(b_psfree);  // dK and dQ^T have read dS^T
           }
         }
         if (!ok) break;
-        mma_commit(b_kvempty);  // K / V of this item are no longer read
-        mma_commit(b_kvout);    // dK / dV accumulators complete
+        mma_commit_warp(b_kvempty);  // K / V of this item are no longer read
+        mma_commit_warp(b_kvout);    // dK / dV accumulators complete
       }
       if (!ok) raise_error(abort_flag);
-      mma_drain(b_drain);
+      mma_drain_warp(b_drain);
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ P^T, dS^T, dK / dV out

@@ -155,7 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the schedule; one elected lane issues (see elect_one).
+    {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       const uint32_t idesc_pv = idesc_bf16_f32(128, p.npv, false, true);
       bool ok = true;
@@ -164,17 +165,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = sbase + (uint32_t)s * kStageBytes;
         const uint64_t dq = smem_desc_sw128(st, 16, 1024);
         const uint64_t dk = smem_desc_sw128(st + kTensorBytes, 16, 1024);
-        for (int kk = 0; kk < p.ksteps; ++kk) {
-          const uint64_t off = (uint64_t)(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
-          mma_ss_nm(tmem + (uint32_t)(256 * b), dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(b_sfull(b));
+        if (elect_one())
+          for (int kk = 0; kk < p.ksteps; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
+            mma_ss_nm(tmem + (uint32_t)(256 * b), dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+        __syncwarp();
+        mma_commit_warp(b_sfull(b));
       };
       auto ready_qk = [&](int k) {
         const int b = k & 1;
-        if (!(ok = mbar_wait(b_qkfull(k & 1), (k >> 1) & 1, abort_flag))) return false;
+        if (!(ok = mbar_wait_warp(b_qkfull(k & 1), (k >> 1) & 1, abort_flag))) return false;
         // S / O of buffer b are free once the epilogue of pair k - 2 has read O
-        if (k >= 2 && !(ok = mbar_wait(b_oempty(b), ((k >> 1) - 1) & 1, abort_flag))) return false;
+        if (k >= 2 && !(ok = mbar_wait_warp(b_oempty(b), ((k >> 1) - 1) & 1, abort_flag))) return false;
         tc_fence_after();
         return true;
       };
@@ -185,19 +188,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ready_qk(k + 1)) break;
           issue_qk(k + 1);
         }
-        if (!(ok = mbar_wait(b_vfull(s), (k >> 1) & 1, abort_flag))) break;
-        if (!(ok = mbar_wait(b_pfull(b), (k >> 1) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(b_vfull(s), (k >> 1) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(b_pfull(b), (k >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         const uint64_t dv = smem_desc_sw128(sbase + (uint32_t)s * kStageBytes + 2 * kTensorBytes,
                                             kChunkBytes, 1024);
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts_nm(tmem + (uint32_t)(256 * b + 128), tmem + (uint32_t)(256 * b + kk * 8),
-                    dv + (uint64_t)(kk * 128), idesc_pv, kk > 0 ? 1u : 0u);
-        mma_commit(b_ofull(b));
-        mma_commit(b_sempty(s));
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts_nm(tmem + (uint32_t)(256 * b + 128), tmem + (uint32_t)(256 * b + kk * 8),
+                      dv + (uint64_t)(kk * 128), idesc_pv, kk > 0 ? 1u : 0u);
+        }
+        __syncwarp();
+        mma_commit_warp(b_ofull(b));
+        mma_commit_warp(b_sempty(s));
       }
       if (!ok) raise_error(abort_flag);
-      mma_drain(b_drain);
+      mma_drain_warp(b_drain);
     }
   } else {
     // ------------------------------------------------------------ softmax warps

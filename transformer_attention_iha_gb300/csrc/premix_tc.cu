@@ -26,7 +26,7 @@
 //              TMA stores of its [32 rows, 64 f] boxes (no cross-warp sync).
 //   warp 8     TMA producer of X: one [64 f, 32 s, d/64, 2 tokens] box per
 //              stage (rows s >= H arrive as zeros), 4-stage ring.
-//   warp 9     MMA issuer (lane 0) and TMEM owner (2 x 256 accumulator
+//   warp 9     MMA issuer (one elected lane) and TMEM owner (2 x 256 accumulator
 //              columns, double-buffered against the epilogue).
 // W (hi | lo) sits in shared memory as a 128 x 64 K-major, 128-byte-swizzled
 // A operand, written once per CTA.
@@ -91,6 +91,16 @@ __device__ __forceinline__ float2 rope_inv_freq(const RopeTable& rt, int i) {
 __device__ __forceinline__ void raise_error(volatile int* abort_flag) {
   *abort_flag = 1;
   atomicOr(&g_dev_error, DEV_ERR_WAIT_TIMEOUT);
+}
+
+// dX chain of the backward: NK K-steps of 16 pseudo-heads; A = dY (MN-major,
+// 2 KB per K-step), B = W^T hi | lo (K-major, 4 K-steps per 8 KB block).
+template <int NK>
+__device__ __forceinline__ void issue_dx(uint32_t d, uint64_t a0, uint64_t b0, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < NK; ++kk)
+    mma_ss_nm(d, a0 + (uint64_t)(kk * 128), b0 + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
+              idesc, kk > 0 ? 1u : 0u);
 }
 
 template <int D>
@@ -200,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the schedule; one elected lane issues (see elect_one).
+    {
       const uint32_t idesc = idesc_bf16_f32(128, kTok * D, false, true);
       const int nks = (p.H + 15) >> 4;
       int k = 0;
@@ -209,21 +220,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tns = G / p.n_stages;
         const uint32_t wt = sW + (uint32_t)tns * p.w_spacing;
         const int xs = k % XS, a = k & 1;
-        if (!(ok = mbar_wait(b_xfull(xs), (k / XS) & 1, abort_flag))) break;
-        if (!(ok = mbar_wait(b_accempty(a), ((k >> 1) & 1) ^ 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(b_xfull(xs), (k / XS) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(b_accempty(a), ((k >> 1) & 1) ^ 1, abort_flag))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(a * 256);
         const uint32_t xbase = sX + xs * p.stage_bytes;
-        int j = 0;
-        for (int part = 0; part < 2; ++part)
-          for (int ks = 0; ks < nks; ++ks, ++j)
-            mma_ss(d_tmem, smem_desc_sw128(wt + part * 64 + ks * 32, 16, 1024),
-                   smem_desc_sw128(xbase + ks * 2048, 32 * 128, 1024), idesc, j > 0 ? 1u : 0u);
-        mma_commit(b_xempty(xs));
-        mma_commit(b_accfull(a));
+        const uint64_t dw0 = smem_desc_sw128(wt, 16, 1024);
+        const uint64_t dx0 = smem_desc_sw128(xbase, 32 * 128, 1024);
+        if (elect_one()) {
+          int j = 0;
+          for (int part = 0; part < 2; ++part)
+            for (int ks = 0; ks < nks; ++ks, ++j)
+              mma_ss_nm(d_tmem, dw0 + (uint64_t)((part * 64 + ks * 32) >> 4),
+                        dx0 + (uint64_t)(ks * 128), idesc, j > 0 ? 1u : 0u);
+        }
+        __syncwarp();
+        mma_commit_warp(b_xempty(xs));
+        mma_commit_warp(b_accfull(a));
       }
       if (!ok) raise_error(abort_flag);
-      mma_drain(b_drain);  // no MMA in flight when TMEM is released
+      mma_drain_warp(b_drain);  // no MMA in flight when TMEM is released
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -614,7 +630,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the schedule; one elected lane issues (see elect_one).
+    {
       const uint32_t idesc_dx = idesc_bf16_f32(128, 64, true, false);
       const uint32_t idesc_dw = idesc_bf16_f32(128, NDW, false, false);
       const int nk_hp = p.hp_pad >> 4;
@@ -632,43 +649,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int k = 0; k < n_my; ++k) {
         const int s = k % NS;
         const uint64_t st16 = (uint64_t)(((uint32_t)s * stage_bytes) >> 4);
-        if (!(ok = mbar_wait(b_infull(s), (k / NS) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(b_infull(s), (k / NS) & 1, abort_flag))) break;
         tc_fence_after();
         if (DO_DX) {
           const int a = k % kBwdNA;
-          if (!(ok = mbar_wait(b_accempty(a), ((k / kBwdNA) & 1) ^ 1, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(b_accempty(a), ((k / kBwdNA) & 1) ^ 1, abort_flag))) break;
           tc_fence_after();
-          for (int kk = 0; kk < nk_hp; ++kk)
-            mma_ss_nm(tmem + (uint32_t)(a * 64), d_dx_a + st16 + (uint64_t)(kk * 128),
-                      d_dx_b + (uint64_t)((((kk >> 2) * 8192) + (kk & 3) * 32) >> 4), idesc_dx,
-                      kk > 0 ? 1u : 0u);
-          mma_commit(b_accfull(a));
+          const uint32_t dxd = tmem + (uint32_t)(a * 64);
+          const uint64_t dxa = d_dx_a + st16;
+          if (elect_one()) switch (nk_hp) {  // a fully unrolled chain
+            case 1: issue_dx<1>(dxd, dxa, d_dx_b, idesc_dx); break;
+            case 2: issue_dx<2>(dxd, dxa, d_dx_b, idesc_dx); break;
+            case 3: issue_dx<3>(dxd, dxa, d_dx_b, idesc_dx); break;
+            case 4: issue_dx<4>(dxd, dxa, d_dx_b, idesc_dx); break;
+            case 5: issue_dx<5>(dxd, dxa, d_dx_b, idesc_dx); break;
+            case 6: issue_dx<6>(dxd, dxa, d_dx_b, idesc_dx); break;
+            case 7: issue_dx<7>(dxd, dxa, d_dx_b, idesc_dx); break;
+            default: issue_dx<8>(dxd, dxa, d_dx_b, idesc_dx); break;
+          }
+          __syncwarp();
+          mma_commit_warp(b_accfull(a));
         }
         if (DO_DW) {
           const int dwc = k / kDwChunk, dwb = dwc & 1;
           const bool dw_first = (k % kDwChunk) == 0;
           if (dw_first && dwc >= 2 &&
-              !(ok = mbar_wait(b_dwempty(dwb), ((dwc >> 1) - 1) & 1, abort_flag))) break;
+              !(ok = mbar_wait_warp(b_dwempty(dwb), ((dwc >> 1) - 1) & 1, abort_flag))) break;
           uint64_t xb = d_dw_b + st16;
           if (PREP) {
-            if (!(ok = mbar_wait(b_xrfull(k & 1), (k >> 1) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait_warp(b_xrfull(k & 1), (k >> 1) & 1, abort_flag))) break;
             tc_fence_after();
             xb = d_dw_b + (uint64_t)((k & 1) * (16384 >> 4));
           }
+          const uint32_t dwd = tmem_dw + (uint32_t)(64 * dwb);
+          const uint64_t dwa0 = d_dw_a + st16, dwa1 = dwa0 + (uint64_t)(chunk >> 4);
+          const uint64_t xb1 = xb + (uint64_t)(xchunk >> 4);
+          const uint32_t acc0 = dw_first ? 0u : 1u;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t aoff = (uint32_t)(kk >> 2) * chunk + (uint32_t)(kk & 3) * 32u;
-            const uint32_t boff = (uint32_t)(kk >> 2) * xchunk + (uint32_t)(kk & 3) * 32u;
-            mma_ss_nm(tmem_dw + (uint32_t)(64 * dwb), d_dw_a + st16 + (uint64_t)(aoff >> 4),
-                      xb + (uint64_t)(boff >> 4), idesc_dw, (!dw_first || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss_nm(dwd, (kk < 4 ? dwa0 : dwa1) + (uint64_t)((kk & 3) * 2),
+                        (kk < 4 ? xb : xb1) + (uint64_t)((kk & 3) * 2), idesc_dw,
+                        kk > 0 ? 1u : acc0);
           }
-          if (PREP) mma_commit(b_xrempty(k & 1));
-          if ((k % kDwChunk) == kDwChunk - 1 || k == n_my - 1) mma_commit(b_dwfull(dwb));
+          __syncwarp();
+          if (PREP) mma_commit_warp(b_xrempty(k & 1));
+          if ((k % kDwChunk) == kDwChunk - 1 || k == n_my - 1) mma_commit_warp(b_dwfull(dwb));
         }
-        mma_commit(b_inempty(s));
+        mma_commit_warp(b_inempty(s));
       }
       if (!ok) raise_error(abort_flag);
-      mma_drain(b_drain);  // no MMA in flight when TMEM is released
+      mma_drain_warp(b_drain);  // no MMA in flight when TMEM is released
     }
   } else if (warp >= 10) {
     // ------------------------------------------------------------ R X (hi / lo)
