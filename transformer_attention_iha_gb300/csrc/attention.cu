@@ -119,6 +119,28 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int idx) {
   return it;
 }
 
+// -inf outside the visible columns [c_lo, c_hi] of a row, for NC chunks of 32
+// scores starting at column c0.  A row's visible columns form one interval
+// and a warp holds 32 consecutive rows, so most chunks are visible (or
+// hidden) for the whole warp: those take a warp-uniform shortcut, and only
+// the chunks the interval edge crosses pay a select per score.
+template <int NC>
+__device__ __forceinline__ void mask_cols(uint32_t* s, int c0, int c_lo, int c_hi) {
+#pragma unroll
+  for (int cc = 0; cc < NC; ++cc) {
+    const int a = c0 + 32 * cc;
+    // visible columns of this chunk, bits lo .. hi - 1
+    const int lo = min(max(c_lo - a, 0), 32), hi = min(max(c_hi - a + 1, 0), 32);
+    const uint32_t vis = (hi >= 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u)) &
+                         ~(lo >= 32 ? 0xFFFFFFFFu : ((1u << lo) - 1u));
+    if (__any_sync(0xffffffffu, vis != 0xFFFFFFFFu)) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        s[32 * cc + e] = (vis >> e) & 1u ? s[32 * cc + e] : 0xFF800000u;
+    }
+  }
+}
+
 __device__ __forceinline__ void raise_error(volatile int* abort_flag) {
   *abort_flag = 1;
   atomicOr(&g_dev_error, DEV_ERR_WAIT_TIMEOUT);
@@ -184,20 +206,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
+    // The whole warp runs the schedule; one elected lane issues (see elect_one).
+    {
+      if (elect_one()) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+      }
+      __syncwarp();
       uint32_t kc = 0, vc = 0, qn0 = 0, qn1 = 0;  // loads issued per ring / Q tile
       bool ok = true;
       // Q tile t of item `it` (qn: loads of that tile so far); returns the new count
       auto load_q = [&](const Item& it, int t, uint32_t qn) -> uint32_t {
-        if (qn > 0 && !(ok = mbar_wait(b_qempty(t), (qn - 1) & 1, abort_flag, lim))) return qn;
-        mbar_arrive_expect_tx(b_qfull(t), kChunkBytes);
+        if (qn > 0 && !(ok = mbar_wait_warp(b_qempty(t), (qn - 1) & 1, abort_flag, lim)))
+          return qn;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(b_qfull(t), kChunkBytes);
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
-          tma_load_5d(sQ + (2 * t + c) * kTileChunkBytes, &tmQ, b_qfull(t), c * kChunk,
-                      (it.qt0 + t) * kBM, it.h, it.bi, it.bo);
+          for (int c = 0; c < NCH; ++c)
+            tma_load_5d(sQ + (2 * t + c) * kTileChunkBytes, &tmQ, b_qfull(t), c * kChunk,
+                        (it.qt0 + t) * kBM, it.h, it.bi, it.bo);
+        }
+        __syncwarp();
         return qn + 1;
       };
       // load number n of the K (is_v = false) or V ring; returns the new count
@@ -206,16 +236,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = (int)(n % depth);
         if (is_v && n == 0 && p.withhold && blockIdx.x == 0)
           return n + 1;  // withheld: its consumer's wait runs out (failure-path test)
-        if (n >= depth && !(ok = mbar_wait(is_v ? b_vempty(s) : b_kempty(s),
-                                           ((n / depth) - 1) & 1, abort_flag, lim)))
+        if (n >= depth && !(ok = mbar_wait_warp(is_v ? b_vempty(s) : b_kempty(s),
+                                                ((n / depth) - 1) & 1, abort_flag, lim)))
           return n;
         const uint32_t full = is_v ? b_vfull(s) : b_kfull(s);
-        mbar_arrive_expect_tx(full, kChunkBytes);
         const uint32_t dst = (is_v ? sV : sK) + (uint32_t)(2 * s) * kTileChunkBytes;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(full, kChunkBytes);
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
-          tma_load_5d(dst + c * kTileChunkBytes, is_v ? &tmV : &tmK, full, c * kChunk, j * kBN,
-                      it.h, it.bi, it.bo);
+          for (int c = 0; c < NCH; ++c)
+            tma_load_5d(dst + c * kTileChunkBytes, is_v ? &tmV : &tmK, full, c * kChunk, j * kBN,
+                        it.h, it.bi, it.bo);
+        }
+        __syncwarp();
         return n + 1;
       };
       for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
@@ -394,11 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s + 32 * c);
           tmem_wait_ld();
-          if (!full_tile) {
-#pragma unroll
-            for (int e = 0; e < 128; ++e)
-              s[e] = sel_u32(e < c_lo || e > c_hi, 0xFF800000u, s[e]);  // -inf outside
-          }
+          if (!full_tile) mask_cols<4>(s, 0, c_lo, c_hi);
           float mx[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) mx[q] = __uint_as_float(s[q]);
@@ -433,11 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tS + 64u * h, s);
           tmem_ld32(tS + 64u * h + 32u, s + 32);
           tmem_wait_ld();
-          if (!full_tile) {
-#pragma unroll
-            for (int e = 0; e < 64; ++e)
-              s[e] = sel_u32(64 * h + e < c_lo || 64 * h + e > c_hi, 0xFF800000u, s[e]);
-          }
+          if (!full_tile) mask_cols<2>(s, 64 * h, c_lo, c_hi);
           uint32_t pk[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
