@@ -23,11 +23,13 @@
 //                           dQ^T = K^T dS^T -> TMA reduce-add into dQ_acc
 //   attn_bwd_post_kernel  dQ = bf16(scale dQ_acc).
 // Roles of the main kernel (320 threads):
-//   warps 0-3  P^T and dS^T (thread = key row = TMEM lane), dK / dV epilogue
-//   warps 4-7  dQ^T drain (thread = feature = TMEM lane): staged in the tile's
+//   warps 0-7  P^T and dS^T (thread = key row = TMEM lane; warps w and w + 4
+//              share the lanes and take query columns 0-63 / 64-127), dK / dV
+//              epilogue (feature columns split the same way)
+//   warps 8-11 dQ^T drain (thread = feature = TMEM lane): staged in the tile's
 //              Q / dO stage, added into dQ_acc by one TMA reduce-add a tile
-//   warp  8    TMA producer (K, V once per item; Q, dO per query tile, 2 stages)
-//   warp  9    tcgen05.mma issuer and TMEM owner
+//   warp  12   TMA producer (K, V once per item; Q, dO per query tile, 2 stages)
+//   warp  13   tcgen05.mma issuer and TMEM owner
 // TMEM (512 columns): regions R0 | R1 rotate S^T / dP^T / dQ^T between query
 // tiles; dK at 256, dV at 384.  One shared 128 x 128 bf16 tile holds P^T,
 // then (in place, once dV has read it) dS^T: rows = keys, 64-query chunks,
@@ -47,7 +49,8 @@ IHA_DEVICE_ERROR_WORD(attention_bwd)
 constexpr int kB = 128;                      // keys (and queries) per tile
 constexpr int kChunkB = kB * 128;            // one 64-wide chunk of a 128-row tile (16 KB)
 constexpr int kTileB = 2 * kChunkB;          // a 128 x 128 bf16 tile (32 KB)
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kCompute = 256;  // threads of warps 0-7
 // shared memory: K | V | Q[2] | dO[2] | P/dS tiles | lse2, D per Q stage |
 // barriers.  No alignment slack fits: the dynamic shared memory must start
 // 1024-byte aligned (it does when the kernel has no static shared memory);
@@ -158,18 +161,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(b_sfull, 1);
     mbar_init(b_dpfull, 1);
-    mbar_init(b_ptfull, 128);
+    mbar_init(b_ptfull, kCompute);
     mbar_init(b_dvdone, 1);
-    mbar_init(b_dsfull, 128);
+    mbar_init(b_dsfull, kCompute);
     mbar_init(b_psfree, 1);
     mbar_init(b_kvout, 1);
-    mbar_init(b_kvoutempty, 128);
+    mbar_init(b_kvoutempty, kCompute);
     mbar_init(b_drain, 1);
     mbar_init(b_stg, 128);
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tDK = tmem + 256u, tDV = tmem + 384u;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t n = nq > 2 ? nq - 2 : 0; n < nq; ++n)
         mbar_wait(b_qfull(n & 1), (n >> 1) & 1, &no_abort);
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the schedule; one elected lane issues (see elect_one).
     {
@@ -313,10 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) raise_error(abort_flag);
       mma_drain_warp(b_drain);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ P^T, dS^T, dK / dV out
-    const int row = warp * 32 + lane;  // key row of the tile = TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int row = (warp & 3) * 32 + lane;  // key row of the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int hf = warp >> 2;                // query columns 64 hf .. 64 hf + 63
     bool ok = true;
     uint32_t ni = 0, gt = 0;
     for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++ni) {
@@ -342,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the P / dS tile is free once the previous tile's dQ^T has read it
         if (gt >= 1 && !(ok = mbar_wait_warp(b_psfree, (gt - 1) & 1, abort_flag))) break;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
           uint32_t sv[32];
           tmem_ld32(tS + 32u * c, sv);
           tmem_wait_ld();
@@ -385,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(b_dvdone, gt & 1, abort_flag))) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
           // fp32 P (phase A left it over S^T in TMEM; a bf16 P here would
           // double the rounding error of dS) and dP
           uint32_t pv[32], dp[32];
@@ -419,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait_warp(b_kvout, ni & 1, abort_flag))) break;
       tc_fence_after();
       const int64_t orow = (((int64_t)it.b * p.N + min(kj, p.N - 1)) * p.Hh + it.h) * p.d;
-      for (int c = 0; c < p.ksteps * 16; c += 32) {
+      for (int c = 32 * hf; c < p.ksteps * 16; c += 64) {
         uint32_t a[32], bv[32];
         tmem_ld32(tDK + lane_base + (uint32_t)c, a);
         tmem_ld32(tDV + lane_base + (uint32_t)c, bv);
@@ -448,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(b_kvoutempty);
     }
     if (!ok) raise_error(abort_flag);
-  } else {
-    // ------------------------------------------------------------ dQ^T drain (warps 4-7)
+  } else if (warp < 12) {
+    // ------------------------------------------------------------ dQ^T drain (warps 8-11)
     // Once dQ^T(t) is complete, every MMA that reads tile t's Q / dO stage
     // has finished, so the stage (64 KB, contiguous) becomes the staging
     // area: rows = queries, d fp32 features each, thread = feature writes its
@@ -457,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // adds the whole tile into dQ_acc with a single TMA reduce-add (box
     // d x 128; the reduction runs in the bulk-copy engine, not as 16 K element
     // atomics) and hands the stage back to the producer once it has been read.
-    const int wq = warp - 4;
+    const int wq = warp - 8;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const int feat = wq * 32 + lane;
     const bool issuer = wq == 0 && lane == 0;
@@ -503,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
