@@ -147,6 +147,7 @@ OP_INPUTS = {
     "mu_gather": ["mu_x", "mu_keep"],
     "mu_attention": ["mu_x", "mu_keep"],
     "mu_scatter": ["mu_x", "mu_keep"],
+    "mu_attention_fused": ["mu_x", "mu_keep"],
     "long_premix_fwd_qkv": [f"l{a}_{t}" for t in "qkv" for a in "xw"],
     "long_attention_causal": [f"l{a}_{t}" for t in "qkv" for a in "xw"],
 }
@@ -242,6 +243,39 @@ class Step:
         T.mha_fwd(self.ly["q"], self.ly["k"], self.ly["v"], mask=T.MASK_CAUSAL, out=self.lo,
                   lse=self.llse)
         done()
+
+
+def extra_ops(T, torch, dev, step, device, iters: int, hbm: float, tc: float):
+    """Ops beyond the step's rows, timed alone after it (not part of `value`):
+    the fused gather -> mask-unit attention -> scatter of the Hiera stage-1
+    step, against its own algorithmic bytes (kept tokens read once from x and
+    written once to the canvas)."""
+    mu = S.HIERA_MU
+    kept = mu.B * mu.n_keep * mu.unit_tokens * mu.C * 2
+    nbytes = 2 * kept + mu.B * mu.n_keep * 4
+    flops = 4 * mu.C * mu.unit_tokens * mu.unit_tokens * mu.B * mu.n_keep
+    canvas = torch.zeros_like(dev["mu_x"])
+    run = lambda: T.mu_attention_fused(dev["mu_x"], dev["mu_keep"], canvas, mu.grid_h, mu.grid_w,
+                                       mu.mu_h, mu.mu_w)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > L2 between launches
+    for _ in range(3):
+        run()
+    ts = []
+    for _ in range(max(iters, 3)):
+        flush.fill_(0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run()
+        e1.record()
+        torch.cuda.synchronize(device)
+        ts.append(e0.elapsed_time(e1))
+    ms = statistics.median(ts)
+    ideal = max(nbytes / hbm, flops / tc)
+    return {"mu_attention_fused": {
+        "ms": round(ms, 5), "roofline_ms": round(ideal * 1e3, 5),
+        "frac": round(ideal / (ms * 1e-3), 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+        "bound": "hbm", "l2": "256 MB written between launches",
+        "replaces": "mu_gather + mu_attention + mu_scatter (one pass, no gathered copy in HBM)"}}
 
 
 class ClockSampler:
@@ -406,6 +440,7 @@ def gpu_arm(args, rank, world, local_rank):
     roof["peak_source"] = f"{peak_src} ({'bf16 burst' if roof['bound'] == 'tensor' else 'copy'})"
 
     tiny = tiny_layer_latency(T, torch, device)
+    extras = extra_ops(T, torch, dev, step, device, args.steps, hbm, tc)
 
     # end to end: host buffers; every input copied in and every result read back per step
     e2e = None
@@ -460,6 +495,7 @@ def gpu_arm(args, rank, world, local_rank):
         "ops": op_out,
         "roofline": roof,
         "tiny_layer_fp32": tiny,
+        "extras": extras,
         "e2e": e2e,
         "gpu_launches": launches_per_step() * args.steps,
         "clocks": clk,
@@ -610,6 +646,10 @@ def single_op(T, torch, name, dev, device):
         return lambda: T.mha_bwd(i["a_q"], i["a_k"], i["a_v"], o, i["a_do"], lse,
                                  mask=T.MASK_CAUSAL_WINDOW, window=S.WINDOW_KEYS, dq=g[0],
                                  dk=g[1], dv=g[2], workspace=ws)
+    if kind == "mu_attention_fused":
+        canvas = torch.zeros_like(i["mu_x"])
+        return lambda: T.mu_attention_fused(i["mu_x"], i["mu_keep"], canvas, mu.grid_h, mu.grid_w,
+                                            mu.mu_h, mu.mu_w)
     if kind.startswith("mu_"):
         g, ou = e((mu.B, mu.n_keep, mu.unit_tokens, mu.C)), e((mu.B, mu.n_keep, mu.unit_tokens, mu.C))
         dec = torch.zeros((mu.B, mu.grid_h * mu.grid_w, mu.C), dtype=torch.bfloat16, device=device)
@@ -659,7 +699,12 @@ def single_op_arm(args):
     torch.cuda.synchronize(device)
     if T.device_error() != 0:
         raise RuntimeError("device error word set")
-    nbytes, flops = {n: (b, f) for n, b, f in op_table()}[args.only]
+    table = {n: (b, f) for n, b, f in op_table()}
+    mu = S.HIERA_MU
+    table["mu_attention_fused"] = (2 * mu.B * mu.n_keep * mu.unit_tokens * mu.C * 2 +
+                                   mu.B * mu.n_keep * 4,
+                                   4 * mu.C * mu.unit_tokens ** 2 * mu.B * mu.n_keep)
+    nbytes, flops = table[args.only]
     ms = e0.elapsed_time(e1) / args.steps
     out = {"op": args.only, "ms": round(ms, 5), "GB/s": round(nbytes / ms / 1e6, 1),
            "bytes": nbytes, "flops": flops, "steps": args.steps, "warmup": args.warmup,

@@ -242,6 +242,27 @@ iha_status mu_scatter(const void* src, const int32_t* keep, void* x, int B,
                       int C, int elem_bytes, void* stream);
 
 /*
+ * Hiera stage-1 attention step in one pass: gather, mask-unit attention and
+ * scatter ("hiera-optim 0.1.0": README item 2 and MaskUnitAttentionFast.forward;
+ * the qkv and proj layers around the attention are not on this path, so
+ * Q = K = V = the unit's tokens).  For every kept unit (b, keep[b,k]):
+ *   canvas[b, tok(u, t), :] = sum_t' softmax_t'(scale x_t . x_t') x_t'
+ * with x_t = x[b, tok(u, t), :], t, t' over the unit's mu_h*mu_w tokens, and
+ * tok() as for mu_gather; every other canvas token is left untouched.  It
+ * equals mu_gather -> mha_fwd (mask none) -> mu_scatter without the
+ * gathered units ever being written to memory.
+ *   x      [B, grid_h*grid_w, C] bf16, dense, 16-byte aligned
+ *   keep   [B, n_keep] int32 unit ids (out-of-range ids: unit skipped,
+ *          iha_device_error() flagged)
+ *   canvas [B, grid_h*grid_w, C] bf16, must not overlap x or keep
+ * Requires mu_h*mu_w <= 64, C % 8 == 0, C <= 128, grid_h % mu_h == 0,
+ * grid_w % mu_w == 0, n_keep <= units; scale <= 0 means C^-1/2.
+ */
+iha_status mu_attention_fused(const void* x, const int32_t* keep, void* canvas, int B,
+                              int grid_h, int grid_w, int mu_h, int mu_w, int n_keep,
+                              int C, float scale, iha_dtype dt, void* stream);
+
+/*
  * Test hook for the failure path; never needed in normal use.  Arms the next
  * bf16 mha_fwd launch made on the calling host thread (one shot) so that
  * CTA 0 withholds the load of its first V tile and every wait of that launch

@@ -33,7 +33,7 @@ MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW = 0, 1, 2
 SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",
            "mha_fwd", "mu_gather", "mu_scatter", "iha_status_string", "iha_last_error",
            "iha_device_error", "iha_test_fail_next_wait", "mha_bwd", "mha_bwd_workspace_bytes",
-           "mha_bwd_noalloc", "iha_premix_fwd_qkv")
+           "mha_bwd_noalloc", "iha_premix_fwd_qkv", "mu_attention_fused")
 
 
 class IHAError(RuntimeError):
@@ -80,9 +80,10 @@ def lib() -> C.CDLL:
     L.mha_bwd_noalloc.restype = C.c_int
     L.mu_gather.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     L.mu_scatter.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
+    L.mu_attention_fused.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
     for name in ("iha_premix_fwd", "iha_premix_fwd_qkv", "iha_premix_bwd_dx",
                  "iha_premix_bwd_dw", "iha_premix_bwd", "mha_fwd", "mha_bwd", "mu_gather",
-                 "mu_scatter"):
+                 "mu_scatter", "mu_attention_fused"):
         getattr(L, name).restype = C.c_int
     L.iha_status_string.argtypes = [i]
     L.iha_status_string.restype = C.c_char_p
@@ -377,6 +378,22 @@ def mu_gather(x, keep, grid_h: int, grid_w: int, mu_h: int, mu_w: int, out=None,
     check(lib().mu_gather(_ptr(x), _ptr(keep), _ptr(out), B, grid_h, grid_w, mu_h, mu_w, n_keep,
                           Cc, x.element_size(), _stream(stream)), "mu_gather")
     return out
+
+
+def mu_attention_fused(x, keep, canvas, grid_h: int, grid_w: int, mu_h: int, mu_w: int,
+                       scale: float = 0.0, stream=None):
+    """Gather -> mask-unit attention (Q = K = V = the unit's tokens) -> scatter
+    into `canvas` (in place; tokens of units not kept are untouched)."""
+    torch = _torch()
+    _mu_check(x, keep, grid_h, grid_w, mu_h, mu_w)
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bfloat16")
+    B, G, Cc = x.shape
+    _expect(canvas, "canvas", (B, G, Cc), x.dtype, x.device)
+    check(lib().mu_attention_fused(_ptr(x), _ptr(keep), _ptr(canvas), B, grid_h, grid_w, mu_h,
+                                   mu_w, keep.shape[1], Cc, float(scale), BF16, _stream(stream)),
+          "mu_attention_fused")
+    return canvas
 
 
 def mu_scatter(src, keep, x, grid_h: int, grid_w: int, mu_h: int, mu_w: int, stream=None):

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "mu_attention.h"
 
 namespace iha {
 namespace {
@@ -258,6 +259,37 @@ iha_status mu_scatter(const void* src, const int32_t* keep, void* x, int B, int 
                       void* stream) {
   return iha::mu_launch<false>(src, keep, x, B, grid_h, grid_w, mu_h, mu_w, n_keep, C,
                                elem_bytes, stream, "mu_scatter");
+}
+
+iha_status mu_attention_fused(const void* x, const int32_t* keep, void* canvas, int B, int grid_h,
+                              int grid_w, int mu_h, int mu_w, int n_keep, int C, float scale,
+                              iha_dtype dt, void* stream) {
+  using namespace iha;
+  const char* name = "mu_attention_fused";
+  if (!x || !keep || !canvas) return fail(IHA_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (B <= 0 || grid_h <= 0 || grid_w <= 0 || mu_h <= 0 || mu_w <= 0 || n_keep <= 0 || C <= 0)
+    return fail(IHA_ERR_INVALID_ARG, "%s: sizes must be positive", name);
+  if (grid_h % mu_h || grid_w % mu_w)
+    return fail(IHA_ERR_INVALID_ARG, "%s: grid not divisible by the mask unit", name);
+  const int64_t units = (int64_t)(grid_h / mu_h) * (grid_w / mu_w);
+  if (n_keep > units) return fail(IHA_ERR_INVALID_ARG, "%s: n_keep > units", name);
+  if (dt != IHA_BF16) return fail(IHA_ERR_UNSUPPORTED, "%s: bf16 only", name);
+  if (mu_h * mu_w > 64 || C % 8 || C > 128 || mu_w > 256 || mu_h > 256)
+    return fail(IHA_ERR_UNSUPPORTED, "%s: needs mu_h*mu_w <= 64, C %% 8 == 0, C <= 128", name);
+  if ((int64_t)B * n_keep > INT32_MAX || (int64_t)B * grid_h * grid_w * C > (1ll << 40))
+    return fail(IHA_ERR_UNSUPPORTED, "%s: problem too large", name);
+  if (!aligned16(x) || !aligned16(canvas) || (reinterpret_cast<uintptr_t>(keep) & 3))
+    return fail(IHA_ERR_ALIGNMENT, "%s: x and canvas must be 16-byte aligned, keep 4", name);
+  const size_t nb = (size_t)B * grid_h * grid_w * C * 2, nk = (size_t)B * n_keep * 4;
+  auto overlaps = [](const void* a, size_t na, const void* b, size_t nbb) {
+    const uintptr_t p0 = reinterpret_cast<uintptr_t>(a), p1 = reinterpret_cast<uintptr_t>(b);
+    return p0 < p1 + nbb && p1 < p0 + na;
+  };
+  if (overlaps(canvas, nb, x, nb) || overlaps(canvas, nb, keep, nk))
+    return fail(IHA_ERR_INVALID_ARG, "%s: canvas overlaps an input", name);
+  if (!(scale > 0.f)) scale = 1.f / sqrtf((float)C);
+  return iha::mu_attention_fused(x, keep, canvas, B, grid_h, grid_w, mu_h, mu_w, n_keep, C, scale,
+                                 reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

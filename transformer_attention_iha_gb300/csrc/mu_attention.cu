@@ -19,6 +19,16 @@
 //   warps 0-3  softmax + epilogue of even pairs (TMEM buffer 0)
 //   warps 4-7  softmax + epilogue of odd pairs (TMEM buffer 1)
 //   warp  8    TMA producer,  warp 9  MMA issuer and TMEM owner
+//
+// Fused mode (FUSED = true): the Hiera stage-1 step gather -> attention ->
+// scatter ("hiera-optim 0.1.0", README, item 2 of what optimize(model) does,
+// and MaskUnitAttentionFast.forward) as one pass.  A kept unit is read
+// straight from the token grid x [B, grid_h, grid_w, C] by one 4-D TMA box
+// (C / 64 chunks x mu_w x mu_h x 1): the box's rows arrive in the in-unit
+// order t = ty * mu_w + tx, the unit layout the gather would have written.
+// The one tile serves as Q, K and V, and each output row goes to its token
+// of the decoder canvas [B, grid_h * grid_w, C], as the scatter would have
+// put it; the gathered units never exist in HBM.
 #include <math.h>
 
 #include <mutex>
@@ -46,7 +56,31 @@ struct MuParams {
   int64_t so_bo, so_bi, so_seq, so_h;
   __nv_bfloat16* o;
   float* lse;
+  // fused mode: unit U = (sample U / n_keep, kept unit keep[U]) of the grid
+  const int32_t* keep;
+  int n_keep, grid_units, units_per_row, mu_h, mu_w, grid_w, B;
+  int64_t G;  // tokens per sample
 };
+
+// Grid coordinates of kept unit U (fused mode); valid = a unit of a sample
+// whose kept-unit id is in range.
+struct GridUnit {
+  int b, x0, y0;
+  bool exists, valid;
+};
+__device__ __forceinline__ GridUnit grid_unit(const MuParams& p, int U) {
+  GridUnit g;
+  g.exists = U < p.n_units;
+  const int UU = g.exists ? U : 0;
+  const int id = __ldg(p.keep + UU);
+  g.valid = g.exists && id >= 0 && id < p.grid_units;
+  const int uid = g.valid ? id : 0;
+  const int uy = uid / p.units_per_row, ux = uid - uy * p.units_per_row;
+  g.b = UU / p.n_keep;
+  g.x0 = ux * p.mu_w;
+  g.y0 = uy * p.mu_h;
+  return g;
+}
 
 struct UnitRef {
   int h, bo, bi, bz;
@@ -69,34 +103,41 @@ __device__ __forceinline__ void raise_error(volatile int* abort_flag) {
   atomicOr(&g_dev_error, DEV_ERR_WAIT_TIMEOUT);
 }
 
+template <bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
     mu_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const MuParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // load stages: Q, K, V of a pair each (2 stages); fused, one tile serves
+  // all three, so the same memory holds 6 stages and loads run further ahead
+  constexpr int NS = FUSED ? 6 : 2;
+  constexpr uint32_t kSStride = FUSED ? (uint32_t)kTensorBytes : (uint32_t)kStageBytes;
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kStageBytes);
   const uint32_t bar0 = smem_u32(bars);
   auto b_qkfull = [&](int s) { return bar0 + 8u * (0 + s); };
-  auto b_vfull = [&](int s) { return bar0 + 8u * (2 + s); };
-  auto b_sempty = [&](int s) { return bar0 + 8u * (4 + s); };
-  auto b_sfull = [&](int b) { return bar0 + 8u * (6 + b); };
-  auto b_pfull = [&](int b) { return bar0 + 8u * (8 + b); };
-  auto b_ofull = [&](int b) { return bar0 + 8u * (10 + b); };
-  auto b_oempty = [&](int b) { return bar0 + 8u * (12 + b); };
-  const uint32_t b_drain = bar0 + 8u * 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  auto b_vfull = [&](int s) { return bar0 + 8u * (NS + s); };
+  auto b_sempty = [&](int s) { return bar0 + 8u * (2 * NS + s); };
+  auto b_sfull = [&](int b) { return bar0 + 8u * (3 * NS + b); };
+  auto b_pfull = [&](int b) { return bar0 + 8u * (3 * NS + 2 + b); };
+  auto b_ofull = [&](int b) { return bar0 + 8u * (3 * NS + 4 + b); };
+  auto b_oempty = [&](int b) { return bar0 + 8u * (3 * NS + 6 + b); };
+  const uint32_t b_drain = bar0 + 8u * (3 * NS + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * NS + 10);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_my = (p.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(b_qkfull(s), 1);
       mbar_init(b_vfull(s), 1);
       mbar_init(b_sempty(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(b_sfull(s), 1);
       mbar_init(b_pfull(s), 128);
       mbar_init(b_ofull(s), 1);
@@ -105,6 +146,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_drain, 1);
     *abort_flag = 0;
     mbar_init_fence();
+  }
+  if (FUSED && p.T < kRows) {
+    // a unit box fills rows 0 .. T-1 of its half; rows T .. 63 are V rows of
+    // keys whose P is 0, so they must hold finite values: zero them once
+    for (int i = threadIdx.x; i < NS * kTensorBytes / 16; i += kThreads)
+      reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -136,21 +184,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       for (; k < n_my; ++k) {
-        const int item = blockIdx.x + k * gridDim.x, s = k & 1;
-        if (k >= 2 && !(ok = mbar_wait(b_sempty(s), ((k >> 1) - 1) & 1, abort_flag))) break;
-        const uint32_t st = sbase + (uint32_t)s * kStageBytes;
-        mbar_arrive_expect_tx(b_qkfull(s), 2 * box_bytes);
-        load_tensor(&tmQ, st, b_qkfull(s), item);
-        load_tensor(&tmK, st + kTensorBytes, b_qkfull(s), item);
-        mbar_arrive_expect_tx(b_vfull(s), box_bytes);
-        load_tensor(&tmV, st + 2 * kTensorBytes, b_vfull(s), item);
+        const int item = blockIdx.x + k * gridDim.x, s = k % NS;
+        if (k >= NS && !(ok = mbar_wait(b_sempty(s), ((k / NS) - 1) & 1, abort_flag))) break;
+        const uint32_t st = sbase + (uint32_t)s * kSStride;
+        if constexpr (FUSED) {
+          // one tile of both units is Q, K and V; a missing or invalid unit
+          // is read from an out-of-range sample, which TMA fills with zeros
+          mbar_arrive_expect_tx(b_qkfull(s), (uint32_t)p.nch * 2u * (uint32_t)p.T * 128u);
+          for (int u = 0; u < 2; ++u) {
+            const GridUnit g = grid_unit(p, 2 * item + u);
+            for (int c = 0; c < p.nch; ++c)
+              tma_load_4d(st + (uint32_t)c * kChunkBytes + (uint32_t)u * kHalfBytes, &tmQ,
+                          b_qkfull(s), c * 64, g.x0, g.y0, g.valid ? g.b : p.B);
+          }
+          mbar_arrive(b_vfull(s));  // V is the same tile: ordered behind Q K^T
+        } else {
+          mbar_arrive_expect_tx(b_qkfull(s), 2 * box_bytes);
+          load_tensor(&tmQ, st, b_qkfull(s), item);
+          load_tensor(&tmK, st + kTensorBytes, b_qkfull(s), item);
+          mbar_arrive_expect_tx(b_vfull(s), box_bytes);
+          load_tensor(&tmV, st + 2 * kTensorBytes, b_vfull(s), item);
+        }
       }
       if (!ok) raise_error(abort_flag);
       // no copy may still be landing when the CTA exits
       volatile int no_abort = 0;
-      for (int kk = k - 2 > 0 ? k - 2 : 0; kk < k; ++kk) {
-        mbar_wait(b_qkfull(kk & 1), (kk >> 1) & 1, &no_abort);
-        mbar_wait(b_vfull(kk & 1), (kk >> 1) & 1, &no_abort);
+      for (int kk = k - NS > 0 ? k - NS : 0; kk < k; ++kk) {
+        mbar_wait(b_qkfull(kk % NS), (kk / NS) & 1, &no_abort);
+        mbar_wait(b_vfull(kk % NS), (kk / NS) & 1, &no_abort);
       }
     }
   } else if (warp == 9) {
@@ -161,10 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_pv = idesc_bf16_f32(128, p.npv, false, true);
       bool ok = true;
       auto issue_qk = [&](int k) {
-        const int s = k & 1, b = k & 1;
-        const uint32_t st = sbase + (uint32_t)s * kStageBytes;
+        const int s = k % NS, b = k & 1;
+        const uint32_t st = sbase + (uint32_t)s * kSStride;
         const uint64_t dq = smem_desc_sw128(st, 16, 1024);
-        const uint64_t dk = smem_desc_sw128(st + kTensorBytes, 16, 1024);
+        const uint64_t dk = smem_desc_sw128(FUSED ? st : st + kTensorBytes, 16, 1024);
         if (elect_one())
           for (int kk = 0; kk < p.ksteps; ++kk) {
             const uint64_t off = (uint64_t)(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
@@ -175,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto ready_qk = [&](int k) {
         const int b = k & 1;
-        if (!(ok = mbar_wait_warp(b_qkfull(k & 1), (k >> 1) & 1, abort_flag))) return false;
+        if (!(ok = mbar_wait_warp(b_qkfull(k % NS), (k / NS) & 1, abort_flag))) return false;
         // S / O of buffer b are free once the epilogue of pair k - 2 has read O
         if (k >= 2 && !(ok = mbar_wait_warp(b_oempty(b), ((k >> 1) - 1) & 1, abort_flag))) return false;
         tc_fence_after();
@@ -183,16 +244,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (n_my > 0 && ready_qk(0)) issue_qk(0);
       for (int k = 0; ok && k < n_my; ++k) {
-        const int s = k & 1, b = k & 1;
+        const int s = k % NS, b = k & 1;
         if (k + 1 < n_my) {
           if (!ready_qk(k + 1)) break;
           issue_qk(k + 1);
         }
-        if (!(ok = mbar_wait_warp(b_vfull(s), (k >> 1) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(b_vfull(s), (k / NS) & 1, abort_flag))) break;
         if (!(ok = mbar_wait_warp(b_pfull(b), (k >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        const uint64_t dv = smem_desc_sw128(sbase + (uint32_t)s * kStageBytes + 2 * kTensorBytes,
-                                            kChunkBytes, 1024);
+        const uint64_t dv = smem_desc_sw128(
+            sbase + (uint32_t)s * kSStride + (FUSED ? 0u : 2u * kTensorBytes), kChunkBytes, 1024);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -273,11 +334,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- epilogue
       if (!(ok = mbar_wait_warp(b_ofull(b), n & 1, abort_flag))) break;
       tc_fence_after();
-      const UnitRef ur = unit_ref(p, 2 * item + u);
-      const bool store = ur.valid && r < p.T;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.o + ur.bo * p.so_bo + ur.bi * p.so_bi +
-                            (int64_t)min(r, p.T - 1) * p.so_seq + ur.h * p.so_h;
+      bool store;
+      __nv_bfloat16* orow;
+      UnitRef ur;
+      if constexpr (FUSED) {
+        // row r of the unit goes to its token of the canvas
+        const GridUnit g = grid_unit(p, 2 * item + u);
+        if (g.exists && !g.valid && r == 0) atomicOr(&g_dev_error, DEV_ERR_KEEP_INDEX);
+        store = g.valid && r < p.T;
+        const int rr = min(r, p.T - 1), ty = rr / p.mu_w, tx = rr - ty * p.mu_w;
+        const int64_t tok = (int64_t)g.b * p.G + (int64_t)(g.y0 + ty) * p.grid_w + g.x0 + tx;
+        orow = p.o + tok * p.d;
+        ur.valid = false;
+      } else {
+        ur = unit_ref(p, 2 * item + u);
+        store = ur.valid && r < p.T;
+        orow = p.o + ur.bo * p.so_bo + ur.bi * p.so_bi + (int64_t)min(r, p.T - 1) * p.so_seq +
+               ur.h * p.so_h;
+      }
       for (int c = 0; c < p.npv; c += 32) {
         uint32_t v[32];
         tmem_ld32(tO + (uint32_t)c, v);
@@ -299,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(b_oempty(b));
-      if (store && p.lse)
+      if (!FUSED && store && p.lse)
         p.lse[((int64_t)ur.bz * p.Hh + ur.h) * p.T + r] =
             l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
@@ -368,15 +443,71 @@ iha_status mu_attention_fwd(const void* q, const void* k, const void* v, void* o
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   std::call_once(g_attr_once, [] {
-    g_attr_err = cudaFuncSetAttribute(mu_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      kSmemBytes);
+    g_attr_err = cudaFuncSetAttribute(mu_attn_kernel<false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (g_attr_err == cudaSuccess)
+      g_attr_err = cudaFuncSetAttribute(mu_attn_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (g_attr_err != cudaSuccess)
     return fail(IHA_ERR_CUDA, "mha_fwd (smem attribute): %s", cudaGetErrorString(g_attr_err));
   int grid = sm_count();
   if (grid > p.n_items) grid = p.n_items;
-  mu_attn_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  mu_attn_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return check_launch("mha_fwd");
+}
+
+iha_status mu_attention_fused(const void* x, const int32_t* keep, void* canvas, int B, int grid_h,
+                              int grid_w, int mu_h, int mu_w, int n_keep, int C, float scale,
+                              cudaStream_t stream) {
+  // x as [B][grid_h][grid_w][C]: box = 64 channels x mu_w x mu_h x 1 sample
+  CUtensorMap mx;
+  {
+    uint64_t dims[4] = {(uint64_t)C, (uint64_t)grid_w, (uint64_t)grid_h, (uint64_t)B};
+    uint64_t st[3] = {(uint64_t)C * 2, (uint64_t)grid_w * C * 2, (uint64_t)grid_h * grid_w * C * 2};
+    uint32_t box[4] = {64, (uint32_t)mu_w, (uint32_t)mu_h, 1};
+    if (encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x), dims, st,
+                     box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return fail(IHA_ERR_CUDA, "mu_attention_fused: tensor map encoding failed");
+  }
+  MuParams p;
+  p.Bo = B;
+  p.Bi = 1;
+  p.Hh = 1;
+  p.T = mu_h * mu_w;
+  p.d = C;
+  p.nch = (C + 63) / 64;
+  p.ksteps = (C + 15) / 16;
+  p.npv = p.ksteps * 16;
+  p.n_units = B * n_keep;
+  p.n_items = (p.n_units + 1) / 2;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.so_bo = p.so_bi = p.so_seq = p.so_h = 0;
+  p.o = static_cast<__nv_bfloat16*>(canvas);
+  p.lse = nullptr;
+  p.keep = keep;
+  p.n_keep = n_keep;
+  p.units_per_row = grid_w / mu_w;
+  p.grid_units = (grid_h / mu_h) * p.units_per_row;
+  p.mu_h = mu_h;
+  p.mu_w = mu_w;
+  p.grid_w = grid_w;
+  p.B = B;
+  p.G = (int64_t)grid_h * grid_w;
+  std::call_once(g_attr_once, [] {
+    g_attr_err = cudaFuncSetAttribute(mu_attn_kernel<false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (g_attr_err == cudaSuccess)
+      g_attr_err = cudaFuncSetAttribute(mu_attn_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (g_attr_err != cudaSuccess)
+    return fail(IHA_ERR_CUDA, "mu_attention_fused (smem attribute): %s",
+                cudaGetErrorString(g_attr_err));
+  int grid = sm_count();
+  if (grid > p.n_items) grid = p.n_items;
+  mu_attn_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(mx, mx, mx, p);
+  return check_launch("mu_attention_fused");
 }
 
 }  // namespace iha

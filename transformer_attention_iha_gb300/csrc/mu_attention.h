@@ -17,4 +17,10 @@ iha_status mu_attention_fwd(const void* q, const void* k, const void* v, void* o
                             const iha_strides& sk, const iha_strides& sv, const iha_strides& so,
                             float scale, cudaStream_t stream);
 
+// Gather -> mask-unit attention (Q = K = V = the unit's tokens) -> scatter
+// into the canvas in one pass (arguments validated by the entry point).
+iha_status mu_attention_fused(const void* x, const int32_t* keep, void* canvas, int B, int grid_h,
+                              int grid_w, int mu_h, int mu_w, int n_keep, int C, float scale,
+                              cudaStream_t stream);
+
 }  // namespace iha
