@@ -247,3 +247,32 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
     lsb = (f >> np.uint32(16)) & np.uint32(1)
     r = ((f + np.uint32(0x7FFF) + lsb) >> np.uint32(16)) << np.uint32(16)
     return r.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- interleaved pseudo-tokens
+def interleave_heads(y: np.ndarray, H: int, P: int) -> np.ndarray:
+    """Premix output [B, N, H*P, d] (rows h*P + p) -> [B, N, P, H, d].
+
+    The interleaved pseudo-token layout of the joint-softmax reading of IHA
+    ("IHA-CUDA", the "interleaved" heads and the softmax "joint" across the
+    P pseudo-heads): pseudo-token n*P + p of head h carries Y[b, n, h*P + p].
+    A pure reordering; no arithmetic.
+    """
+    B, N, HP, d = y.shape
+    assert HP == H * P
+    return np.ascontiguousarray(y.reshape(B, N, H, P, d).transpose(0, 1, 3, 2, 4))
+
+
+def joint_attention(yq: np.ndarray, yk: np.ndarray, yv: np.ndarray, causal: bool = True,
+                    scale: float | None = None):
+    """Attention of each head h over the N*P interleaved pseudo-tokens
+    m = n*P + p of [B, N, P, H, d] inputs (causal on m when `causal`), by
+    the plain two-pass softmax of ``attention`` on the [B, 1, N*P, H, d] view.
+
+    Returns O [B, N, P, H, d] float64 and lse [B, H, N*P] float64.
+    """
+    B, N, P, H, d = yq.shape
+    view = lambda a: np.ascontiguousarray(a).reshape(B, 1, N * P, H, d)
+    o, lse = attention(view(yq), view(yk), view(yv), MASK_CAUSAL if causal else MASK_NONE, 0,
+                       scale)
+    return o.reshape(B, N, P, H, d), lse.reshape(B, H, N * P)

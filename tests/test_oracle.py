@@ -487,3 +487,51 @@ def test_attention_bwd_absolute_terms_bound_the_gradients():
     _, _, dv = O.attention_bwd(q, k, v, gp, 1, 0)
     _, _, av = O.attention_bwd(q, k, v, gp, 1, 0, absolute=True)
     np.testing.assert_allclose(dv, av, rtol=1e-12)
+
+
+# ---------------------------------------------------------------- interleaved pseudo-tokens
+def test_interleave_heads_orders_pseudo_tokens_n_major():
+    """Row h*P + p of token n becomes pseudo-token (n, p) of head h; P = 1 is
+    the identity."""
+    B, N, H, P, d = 2, 3, 4, 3, 2
+    y = np.arange(B * N * H * P * d, dtype=np.float64).reshape(B, N, H * P, d)
+    z = O.interleave_heads(y, H, P)
+    for b in range(B):
+        for n in range(N):
+            for h in range(H):
+                for p in range(P):
+                    np.testing.assert_array_equal(z[b, n, p, h], y[b, n, h * P + p])
+    y1 = np.arange(24, dtype=np.float64).reshape(1, 3, 4, 2)
+    np.testing.assert_array_equal(O.interleave_heads(y1, 4, 1)[:, :, 0], y1)
+
+
+def test_joint_attention_brute_force():
+    """The joint softmax, written out with loops on a tiny case: query
+    pseudo-token m = n*P + p of head h sees keys m' <= m of the same head."""
+    rng = np.random.default_rng(7)
+    B, N, P, H, d = 2, 3, 2, 2, 4
+    q, k, v = (rng.standard_normal((B, N, P, H, d)).astype(np.float32) for _ in range(3))
+    o, lse = O.joint_attention(q, k, v, causal=True)
+    scale = 1.0 / math.sqrt(d)
+    M = N * P
+    for b in range(B):
+        for h in range(H):
+            for m in range(M):
+                n, p = divmod(m, P)
+                s = np.array([scale * float(np.dot(q[b, n, p, h].astype(np.float64),
+                                                   k[b, m2 // P, m2 % P, h].astype(np.float64)))
+                              for m2 in range(m + 1)])
+                w = np.exp(s - s.max())
+                ref = sum(w[m2] * v[b, m2 // P, m2 % P, h].astype(np.float64)
+                          for m2 in range(m + 1)) / w.sum()
+                np.testing.assert_allclose(o[b, n, p, h], ref, rtol=1e-12, atol=1e-12)
+                assert abs(lse[b, h, m] - (s.max() + math.log(w.sum()))) < 1e-12
+    # no mask: every pseudo-token sees all N*P of its head
+    o2, _ = O.joint_attention(q, k, v, causal=False)
+    b, h, n, p = 1, 0, 0, 1
+    s = np.array([scale * float(np.dot(q[b, n, p, h].astype(np.float64),
+                                       k[b, m2 // P, m2 % P, h].astype(np.float64)))
+                  for m2 in range(M)])
+    w = np.exp(s - s.max())
+    ref = sum(w[m2] * v[b, m2 // P, m2 % P, h].astype(np.float64) for m2 in range(M)) / w.sum()
+    np.testing.assert_allclose(o2[b, n, p, h], ref, rtol=1e-12, atol=1e-12)
