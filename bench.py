@@ -271,11 +271,51 @@ def extra_ops(T, torch, dev, step, device, iters: int, hbm: float, tc: float):
         ts.append(e0.elapsed_time(e1))
     ms = statistics.median(ts)
     ideal = max(nbytes / hbm, flops / tc)
-    return {"mu_attention_fused": {
+    out = {"mu_attention_fused": {
         "ms": round(ms, 5), "roofline_ms": round(ideal * 1e3, 5),
         "frac": round(ideal / (ms * 1e-3), 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
         "bound": "hbm", "l2": "256 MB written between launches",
         "replaces": "mu_gather + mu_attention + mu_scatter (one pass, no gathered copy in HBM)"}}
+    del canvas, flush
+    # joint-softmax variant of the layer forward at the LLaMA shape: premix Q,
+    # K (RoPE), V into the interleaved layout, then causal attention of the 20
+    # heads over the N*P = 32768 pseudo-tokens
+    pm = S.LLAMA_PREMIX
+    ys = tuple(torch.empty((pm.B, pm.N, pm.P, pm.H, pm.d), dtype=torch.bfloat16, device=device)
+               for _ in range(3))
+    o = torch.empty((pm.B, pm.N * pm.P, pm.H, pm.d), dtype=torch.bfloat16, device=device)
+    M = pm.N * pm.P
+    pre = lambda: T.premix_fwd_qkv_interleaved([dev[f"x_{t}"] for t in "qkv"],
+                                               [dev[f"w_{t}"] for t in "qkv"], pm.P, rope=True,
+                                               rope_base=S.ROPE_BASE, out=ys)
+    att = lambda: T.mha_fwd(*(y.view(pm.B, M, pm.H, pm.d) for y in ys), mask=T.MASK_CAUSAL,
+                            out=o)
+    for _ in range(2):
+        pre()
+        att()
+    tp, ta = [], []
+    for _ in range(max(iters // 2, 3)):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        pre()
+        e[1].record()
+        att()
+        e[2].record()
+        torch.cuda.synchronize(device)
+        tp.append(e[0].elapsed_time(e[1]))
+        ta.append(e[1].elapsed_time(e[2]))
+    mp, ma = statistics.median(tp), statistics.median(ta)
+    tok = pm.B * pm.N
+    pbytes = 3 * (tok * pm.H * pm.d * 2 + tok * pm.HP * pm.d * 2 + pm.HP * pm.H * 4)
+    aflops = 4 * pm.d * (M * (M + 1) // 2) * pm.H * pm.B
+    out["iha_joint_softmax_layer"] = {
+        "config": "B=1, N=8192, H=20, P=4, d=128: premix Q,K(+RoPE),V -> [B,N,P,H,d]; causal "
+                  "attention of 20 heads over N*P=32768 pseudo-tokens",
+        "premix_ms": round(mp, 5), "premix_GB/s": round(pbytes / (mp * 1e-3) / 1e9, 1),
+        "premix_frac": round(pbytes / hbm / (mp * 1e-3), 4),
+        "attention_ms": round(ma, 5), "attention_TFLOP/s": round(aflops / (ma * 1e-3) / 1e12, 1),
+        "attention_frac": round(aflops / tc / (ma * 1e-3), 4)}
+    return out
 
 
 class ClockSampler:

@@ -103,6 +103,24 @@ iha_status iha_premix_fwd_qkv(const void* xq, const void* xk, const void* xv,
                               int d, iha_dtype dt, int rope, float rope_base, void* stream);
 
 /*
+ * Premix forward of Q, K and V with the interleaved pseudo-token layout of
+ * the joint-softmax reading of Interleaved Head Attention ("IHA-CUDA", the
+ * "interleaved" head layout and the softmax "joint" across pseudo-heads):
+ *   y_t[b, n, p, h, f] = sum_s w_t[h, p, s] * x_t[b, n, s, f]  (+ RoPE at n)
+ * i.e. the values of iha_premix_fwd_qkv with rows ordered p * H + h instead
+ * of h * P + p.  Viewed as [B, N*P, H, d] (sequence stride H*d, head stride
+ * d), it is an H-head sequence of N*P pseudo-tokens, pseudo-token n*P + p,
+ * which mha_fwd attends over in place (causal on n*P + p).
+ * bf16 only, d in {64, 128}, H <= 32, H*P <= 128; other limits as
+ * iha_premix_fwd_qkv.
+ */
+iha_status iha_premix_fwd_qkv_interleaved(const void* xq, const void* xk, const void* xv,
+                                          const float* wq, const float* wk, const float* wv,
+                                          void* yq, void* yk, void* yv, int B, int N, int H,
+                                          int P, int d, iha_dtype dt, int rope,
+                                          float rope_base, void* stream);
+
+/*
  * Premix input gradient ("Pseudo-Token Mixing", backward, dX = W^T dY):
  *   dx[b,n,s,f] = sum_{h,p} w[h,p,s] * g[b,n,h*P+p,f]
  * with g = dy, or g = R_n^T dy (inverse rotation) when rope != 0.

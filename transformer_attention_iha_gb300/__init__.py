@@ -33,7 +33,8 @@ MASK_NONE, MASK_CAUSAL, MASK_CAUSAL_WINDOW = 0, 1, 2
 SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_premix_bwd",
            "mha_fwd", "mu_gather", "mu_scatter", "iha_status_string", "iha_last_error",
            "iha_device_error", "iha_test_fail_next_wait", "mha_bwd", "mha_bwd_workspace_bytes",
-           "mha_bwd_noalloc", "iha_premix_fwd_qkv", "mu_attention_fused")
+           "mha_bwd_noalloc", "iha_premix_fwd_qkv", "mu_attention_fused",
+           "iha_premix_fwd_qkv_interleaved")
 
 
 class IHAError(RuntimeError):
@@ -67,6 +68,7 @@ def lib() -> C.CDLL:
     vp, i, f = C.c_void_p, C.c_int, C.c_float
     L.iha_premix_fwd.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.iha_premix_fwd_qkv.argtypes = [vp] * 9 + [i, i, i, i, i, i, i, f, vp]
+    L.iha_premix_fwd_qkv_interleaved.argtypes = [vp] * 9 + [i, i, i, i, i, i, i, f, vp]
     L.iha_premix_bwd_dx.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.iha_premix_bwd_dw.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp]
     L.iha_premix_bwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
@@ -81,7 +83,8 @@ def lib() -> C.CDLL:
     L.mu_gather.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     L.mu_scatter.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     L.mu_attention_fused.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
-    for name in ("iha_premix_fwd", "iha_premix_fwd_qkv", "iha_premix_bwd_dx",
+    for name in ("iha_premix_fwd", "iha_premix_fwd_qkv", "iha_premix_fwd_qkv_interleaved",
+                 "iha_premix_bwd_dx",
                  "iha_premix_bwd_dw", "iha_premix_bwd", "mha_fwd", "mha_bwd", "mu_gather",
                  "mu_scatter", "mu_attention_fused"):
         getattr(L, name).restype = C.c_int
@@ -198,6 +201,35 @@ def premix_fwd_qkv(xs, ws, P: int, rope: bool = False, rope_base: float = 10000.
     check(lib().iha_premix_fwd_qkv(*(_ptr(x) for x in xs), *(_ptr(w) for w in ws),
                                    *(_ptr(y) for y in out), B, N, H, P, d, _dt(x0), int(rope),
                                    float(rope_base), _stream(stream)), "iha_premix_fwd_qkv")
+    return tuple(out)
+
+
+def premix_fwd_qkv_interleaved(xs, ws, P: int, rope: bool = False, rope_base: float = 10000.0,
+                               out=None, stream=None):
+    """(Y_q, Y_k, Y_v) as [B, N, P, H, d]: the premix of (X_q, X_k, X_v) with
+    rows ordered p * H + h (the interleaved pseudo-token layout); RoPE on Q, K."""
+    torch = _torch()
+    if len(xs) != 3 or len(ws) != 3:
+        raise ValueError("xs and ws must hold three tensors (q, k, v)")
+    x0 = xs[0]
+    _expect(x0, "xq")
+    if x0.dim() != 4:
+        raise ValueError("x must be [B, N, H, d]")
+    B, N, H, d = x0.shape
+    for t, (x, w) in enumerate(zip(xs, ws)):
+        _expect(x, f"x[{t}]", (B, N, H, d), x0.dtype, x0.device)
+        _expect(w, f"w[{t}]", (H, P, H), torch.float32, x0.device)
+    if out is None:
+        out = tuple(torch.empty((B, N, P, H, d), dtype=x0.dtype, device=x0.device)
+                    for _ in range(3))
+    if len(out) != 3:
+        raise ValueError("out must hold three tensors")
+    for t, y in enumerate(out):
+        _expect(y, f"out[{t}]", (B, N, P, H, d), x0.dtype, x0.device)
+    check(lib().iha_premix_fwd_qkv_interleaved(*(_ptr(x) for x in xs), *(_ptr(w) for w in ws),
+                                               *(_ptr(y) for y in out), B, N, H, P, d, _dt(x0),
+                                               int(rope), float(rope_base), _stream(stream)),
+          "iha_premix_fwd_qkv_interleaved")
     return tuple(out)
 
 

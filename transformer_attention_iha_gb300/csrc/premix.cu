@@ -625,6 +625,35 @@ iha_status iha_premix_fwd_qkv(const void* xq, const void* xk, const void* xv, co
   return IHA_OK;
 }
 
+iha_status iha_premix_fwd_qkv_interleaved(const void* xq, const void* xk, const void* xv,
+                                          const float* wq, const float* wk, const float* wv,
+                                          void* yq, void* yk, void* yv, int B, int N, int H, int P,
+                                          int d, iha_dtype dt, int rope, float rope_base,
+                                          void* stream) {
+  using namespace iha;
+  const void* x[3] = {xq, xk, xv};
+  const float* w[3] = {wq, wk, wv};
+  void* y[3] = {yq, yk, yv};
+  for (int t = 0; t < 3; ++t) {
+    iha_status st = check_common("iha_premix_fwd_qkv_interleaved", x[t], w[t], y[t], B, N, H, P,
+                                 d, dt, t < 2 ? rope : 0, rope_base);
+    if (st != IHA_OK) return st;
+  }
+  if (dt != IHA_BF16 || !premix_tc_supported(H, P, d))
+    return fail(IHA_ERR_UNSUPPORTED,
+                "iha_premix_fwd_qkv_interleaved: bf16 with d in {64, 128}, H <= 32, H*P <= 128");
+  const PremixGeom g = make_geom(B, N, H, P, d, rope_base);
+  const size_t ny = g.ntok * g.HP * d * 2, nx = g.ntok * H * d * 2, nw = (size_t)g.HP * H * 4;
+  for (int t = 0; t < 3; ++t)
+    for (int u = 0; u < 3; ++u)
+      if (overlaps(y[t], ny, x[u], nx) || overlaps(y[t], ny, w[u], nw) ||
+          (u != t && overlaps(y[t], ny, y[u], ny)))
+        return fail(IHA_ERR_INVALID_ARG,
+                    "iha_premix_fwd_qkv_interleaved: an output overlaps another tensor");
+  return premix_fwd_tc_multi(3, x, w, y, B, N, H, P, d, rope ? 3 : 0, rope_base,
+                             reinterpret_cast<cudaStream_t>(stream), 1);
+}
+
 iha_status iha_premix_bwd_dx(const void* dy, const float* w, void* dx, int B, int N, int H,
                              int P, int d, iha_dtype dt, int rope, float rope_base,
                              void* stream) {

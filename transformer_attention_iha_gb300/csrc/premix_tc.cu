@@ -50,6 +50,7 @@ constexpr int kMaxTens = 3;
 struct FwdParams {
   int ntok, N, H, HP, d, nch, n_stages;  // n_stages: token pairs per tensor
   int ntens, rope_mask;                  // tensors of the launch; bit t: RoPE on tensor t
+  int interleave;                        // output rows p * H + h instead of h * P + p
   int x_stages;                          // depth of the X ring (<= kXStages)
   uint32_t stage_bytes;                  // X bytes per stage
   uint32_t w_spacing;                    // bytes between the weight tiles
@@ -155,6 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int idx = tid; idx < p.ntens * rows8 * 8; idx += kEpiThreads) {
       const int tns = idx / (rows8 * 8), r = idx - tns * rows8 * 8;
       const int row = r >> 3, j = r & 7;
+      // weight row of output row `row`: (h, p) = (row / P, row % P), or
+      // interleaved (row % H, row / H)
+      const int wrow = p.interleave ? (row % p.H) * (p.HP / p.H) + row / p.H : row;
       const float* w = p.w[0];
       if (tns == 1) w = p.w[1];
       if (tns == 2) w = p.w[2];
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h2 = 0; h2 < 2; ++h2) {
           const int k = 8 * j + 2 * e + h2;  // 0..63
           const int s = k & 31;
-          const float wv = (row < p.HP && s < p.H) ? __ldg(w + row * p.H + s) : 0.f;
+          const float wv = (row < p.HP && s < p.H) ? __ldg(w + wrow * p.H + s) : 0.f;
           const float hi = __bfloat162float(__float2bfloat16_rn(wv));
           part[h2] = (k < 32) ? hi : (wv - hi);
         }
@@ -369,8 +373,9 @@ void make_rope_table(RopeTable* rt, int d, float base) {
 
 iha_status premix_fwd_tc_multi(int ntens, const void* const* x, const float* const* w,
                                void* const* y, int B, int N, int H, int P, int d, int rope_mask,
-                               float rope_base, cudaStream_t stream) {
+                               float rope_base, cudaStream_t stream, int interleave) {
   FwdParams p;
+  p.interleave = interleave;
   p.ntok = B * N;
   p.N = N;
   p.H = H;

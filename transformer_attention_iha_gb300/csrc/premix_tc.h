@@ -35,8 +35,9 @@ iha_status premix_fwd_tc(const void* x, const float* w, void* y, int B, int N, i
 
 // The same forward over ntens (1..3) tensors in one launch; tensor t reads
 // x[t], w[t], writes y[t], and is rotated when bit t of rope_mask is set.
+// interleave: Y rows ordered p * H + h ([B, N, P, H, d]) instead of h * P + p.
 iha_status premix_fwd_tc_multi(int ntens, const void* const* x, const float* const* w,
                                void* const* y, int B, int N, int H, int P, int d, int rope_mask,
-                               float rope_base, cudaStream_t stream);
+                               float rope_base, cudaStream_t stream, int interleave = 0);
 
 }  // namespace iha
