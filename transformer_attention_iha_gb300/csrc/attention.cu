@@ -47,8 +47,10 @@ constexpr int kBN = 128;             // keys per tile
 constexpr int kChunk = 64;           // head-dim elements per 128-byte swizzle row
 constexpr int kTileChunkBytes = kBM * 128;  // 16 KB: 128 rows x 64 bf16
 constexpr int kThreads = 320;
-constexpr int kKSlots = 3;           // K ring depth (V ring: 2)
-constexpr int kSmemTiles = (4 + 2 * kKSlots + 4) * kTileChunkBytes;  // Q 2x2, K 3x2, V 2x2 chunks
+constexpr int kKSlots = 2;           // K ring depth (V ring: 2)
+constexpr int kStgBytes = 32 * 128;  // per softmax warp: 32 rows x 64 bf16 of O
+// Q 2x2, K 2x2, V 2x2 chunks | O staging of the 8 softmax warps
+constexpr int kSmemTiles = (4 + 2 * kKSlots + 4) * kTileChunkBytes + 8 * kStgBytes;
 constexpr int kSmemBytes = kSmemTiles + 256 + 1024;  // + barriers + alignment slack
 constexpr float kRescaleLog2 = 8.0f;
 // L2 budget for the K / V of one head group.
@@ -151,13 +153,15 @@ template <int NCH>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmO, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sQ = smem_u32(smem);                       // [tile][chunk]
-  const uint32_t sK = sQ + 4 * kTileChunkBytes;             // [slot][chunk], 3 slots
+  const uint32_t sK = sQ + 4 * kTileChunkBytes;             // [slot][chunk], 2 slots
   const uint32_t sV = sK + 2 * kKSlots * kTileChunkBytes;   // [slot][chunk], 2 slots
+  const uint32_t sStg = sV + 4 * kTileChunkBytes;          // [softmax warp][32 rows][128 B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemTiles);
   const uint32_t bar0 = smem_u32(bars);
   auto b_qfull = [&](int t) { return bar0 + 8u * (0 + t); };
@@ -505,28 +509,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++on;
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow =
-          p.o + it.bo * p.so_bo + it.bi * p.so_bi + (int64_t)min(i, p.Nq - 1) * p.so_seq +
-          it.h * p.so_h;
+      // O rows of this warp (32 queries) go out by TMA: normalised, packed
+      // to bf16 into the warp's 128-byte-swizzled staging, one store per 64
+      // columns (rows past Nq and columns past d are clipped by the store)
+      const int i0 = qt * kBM + (warp & 3) * 32;
+      const uint32_t stg = sStg + (uint32_t)warp * kStgBytes;
+      uint8_t* stg_p = smem + (stg - sQ);
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {  // 64 columns of O at a time
         uint32_t r[64];
         tmem_ld32(tO + 64u * c, r);
         tmem_ld32(tO + 64u * c + 32u, r + 32);
         tmem_wait_ld();
-        if (i < p.Nq) {
+        if (lane == 0) bulk_wait_read<0>();  // the previous store has read the staging
+        __syncwarp();
 #pragma unroll
-          for (int g8 = 0; g8 < 8; ++g8) {
-            const int f = 64 * c + 8 * g8;
-            if (f < p.d) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[8 * g8 + 0]) * inv_l, __uint_as_float(r[8 * g8 + 1]) * inv_l);
-              v.y = pack_bf16x2(__uint_as_float(r[8 * g8 + 2]) * inv_l, __uint_as_float(r[8 * g8 + 3]) * inv_l);
-              v.z = pack_bf16x2(__uint_as_float(r[8 * g8 + 4]) * inv_l, __uint_as_float(r[8 * g8 + 5]) * inv_l);
-              v.w = pack_bf16x2(__uint_as_float(r[8 * g8 + 6]) * inv_l, __uint_as_float(r[8 * g8 + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(orow + f) = v;
-            }
-          }
+        for (int g8 = 0; g8 < 8; ++g8) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(r[8 * g8 + 0]) * inv_l, __uint_as_float(r[8 * g8 + 1]) * inv_l);
+          v.y = pack_bf16x2(__uint_as_float(r[8 * g8 + 2]) * inv_l, __uint_as_float(r[8 * g8 + 3]) * inv_l);
+          v.z = pack_bf16x2(__uint_as_float(r[8 * g8 + 4]) * inv_l, __uint_as_float(r[8 * g8 + 5]) * inv_l);
+          v.w = pack_bf16x2(__uint_as_float(r[8 * g8 + 6]) * inv_l, __uint_as_float(r[8 * g8 + 7]) * inv_l);
+          *reinterpret_cast<uint4*>(stg_p + lane * 128 + ((g8 ^ (lane & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && i0 < p.Nq) {
+          tma_store_5d(&tmO, stg, c * kChunk, i0, it.h, it.bi, it.bo);
+          bulk_commit();
         }
       }
       tc_fence_before();  // O may be overwritten once the next P of this tile is published
@@ -536,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             l > 0.f ? (base + log2f(l)) * 0.6931471805599453f : -INFINITY;
       }
     }
+    if (lane == 0) bulk_wait<0>();  // O stores complete before the CTA exits
     if (!ok) raise_error(abort_flag);
   }
 
@@ -635,7 +646,7 @@ bool stride_ok(const iha_strides& s, int64_t elem) {
 // 128-byte swizzle.  Strides of size-1 dimensions are replaced by a harmless
 // aligned value.
 CUresult make_map(CUtensorMap* m, const void* base, int Bo, int Bi, int N, int Hh, int d,
-                  const iha_strides& s) {
+                  const iha_strides& s, int box_rows = kBM) {
   uint64_t dims[5] = {(uint64_t)d, (uint64_t)N, (uint64_t)Hh, (uint64_t)Bi, (uint64_t)Bo};
   uint64_t st[4] = {(uint64_t)s.seq * 2, (uint64_t)s.head * 2, (uint64_t)s.b_inner * 2,
                     (uint64_t)s.b_outer * 2};
@@ -643,7 +654,7 @@ CUresult make_map(CUtensorMap* m, const void* base, int Bo, int Bi, int N, int H
   if (Hh == 1) st[1] = 16;
   if (Bi == 1) st[2] = 16;
   if (Bo == 1) st[3] = 16;
-  uint32_t box[5] = {(uint32_t)kChunk, (uint32_t)kBM, 1, 1, 1};
+  uint32_t box[5] = {(uint32_t)kChunk, (uint32_t)box_rows, 1, 1, 1};
   return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, st, box,
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -669,9 +680,11 @@ iha_status launch_tc(const void* q, const void* k, const void* v, void* o, float
                      const iha_strides& sk, const iha_strides& sv, const iha_strides& so,
                      float scale, int mask, int window, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
+  CUtensorMap mo;
   if (make_map(&mq, q, Bo, Bi, Nq, Hh, d, sq) != CUDA_SUCCESS ||
       make_map(&mk, k, Bo, Bi, Nk, Hh, d, sk) != CUDA_SUCCESS ||
-      make_map(&mv, v, Bo, Bi, Nk, Hh, d, sv) != CUDA_SUCCESS)
+      make_map(&mv, v, Bo, Bi, Nk, Hh, d, sv) != CUDA_SUCCESS ||
+      make_map(&mo, o, Bo, Bi, Nq, Hh, d, so, 32) != CUDA_SUCCESS)
     return fail(IHA_ERR_CUDA, "mha_fwd: tensor map encoding failed");
   AttnParams p;
   p.Bo = Bo;
@@ -707,9 +720,9 @@ iha_status launch_tc(const void* q, const void* k, const void* v, void* o, float
   int grid = sm_count();
   if (grid > p.n_items) grid = p.n_items;
   if (p.nD == 1)
-    attn_fwd_tc_kernel<1><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    attn_fwd_tc_kernel<1><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mo, p);
   else
-    attn_fwd_tc_kernel<2><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+    attn_fwd_tc_kernel<2><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mo, p);
   return check_launch("mha_fwd");
 }
 

@@ -177,6 +177,14 @@ __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int 
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_5d(const void* map, uint32_t src, int c0, int c1,
+                                             int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
 // Tiled bulk reduce-add from shared memory into global (element type of the
 // tensor map; fp32 here), bulk-group completion like a store.
 __device__ __forceinline__ void tma_reduce_add_4d(const void* map, uint32_t src, int c0, int c1,
