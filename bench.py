@@ -57,7 +57,7 @@ CPU_FRAC = 1 / 256
 # DRAM bytes (read + write) per launch of the dominant kernel, from the one-pass
 # ncu capture in profiles/attn_fwd_tc_causal_B2_N16384_80h_dram.md (removed
 # whenever that kernel changes, until it is captured again).
-NCU_TRAFFIC = {"long_attention_causal": 10743784960 + 673385216}
+NCU_TRAFFIC = {"long_attention_causal": 10517708800 + 673674496}
 
 
 def load_peaks():
