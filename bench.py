@@ -485,27 +485,56 @@ def gpu_arm(args, rank, world, local_rank):
     # end to end: host buffers; every input copied in and every result read back per step
     e2e = None
     if args.e2e_steps > 0:
+        # Every step copies its inputs in from pinned host memory and its
+        # results back out.  Copies and compute run on their own streams over
+        # two sets of device buffers, so step i + 1's inputs arrive (and step
+        # i - 1's results leave) while step i computes, as a training loop
+        # with prefetching would run it.
         pinned = {k: v.pin_memory() for k, v in hostt.items()}
+        dev2 = {k: torch.empty_like(v) for k, v in dev.items()}
+        steps2 = [step, Step(T, torch, dev2, device)]
+        devs = [dev, dev2]
         res_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in step.results()]
         h2d = sum(v.numel() * v.element_size() for v in pinned.values())
         d2h = sum(o.numel() * o.element_size() for o in res_host)
+        s_in, s_run, s_out = (torch.cuda.Stream(device) for _ in range(3))
+        ev = lambda: torch.cuda.Event()
+        in_done, run_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        used = [False, False]
 
-        def e2e_step():
-            for k, v in pinned.items():
-                dev[k].copy_(v, non_blocking=True)
-            step.run()
-            for o, h in zip(step.results(), res_host):
-                h.copy_(o, non_blocking=True)
+        def e2e_step(i):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                if used[b]:
+                    s_in.wait_event(run_done[b])       # step i - 2 has read these inputs
+                for k, v in pinned.items():
+                    devs[b][k].copy_(v, non_blocking=True)
+                in_done[b].record(s_in)
+            with torch.cuda.stream(s_run):
+                s_run.wait_event(in_done[b])
+                if used[b]:
+                    s_run.wait_event(out_done[b])      # step i - 2's results have left
+                steps2[b].run()
+                run_done[b].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(run_done[b])
+                for o, h in zip(steps2[b].results(), res_host):
+                    h.copy_(o, non_blocking=True)
+                out_done[b].record(s_out)
+            used[b] = True
 
-        e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize(device)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             torch.distributed.barrier()
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_in)
+        s_run.wait_event(e0)
+        s_out.wait_event(e0)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        e1.record(s_out)
         torch.cuda.synchronize(device)
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
         if world > 1:
@@ -762,7 +791,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-frac", type=float, default=CPU_FRAC,
                     help="fraction of every op each oracle sample runs")
     ap.add_argument("--cpu-samples", type=int, default=2,
