@@ -76,6 +76,23 @@ def _attn_pairs(N: int, mask: str, W: int = 0) -> int:
     return sum(min(i + 1, W) for i in range(N))
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The job's time: the largest x over the ranks (x itself at world 1).
+    Every rank runs the same replica of the step, so the job processed
+    world x one step's work in that time."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ideal_step_s: float, step_ms: float, world: int) -> float:
+    """`value`: % of the 1-GPU roofline summed over the replicas."""
+    return round(100.0 * ideal_step_s / (step_ms * 1e-3) * world, 3)
+
+
 def op_table():
     """(name, bytes, flops) per op of one step, algorithmic (inputs read once,
     outputs written once)."""
@@ -439,11 +456,7 @@ def gpu_arm(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    total_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(end), world, device)
     ms_step = total_ms / args.steps
     op_ms = [statistics.mean(evs[s][k].elapsed_time(evs[s][k + 1]) for s in range(args.steps))
              for k in range(nops)]
@@ -461,7 +474,6 @@ def gpu_arm(args, rank, world, local_rank):
         if flops:
             rec["TFLOP/s"] = round(flops / (ms * 1e-3) / 1e12, 1)
         op_out[name] = rec
-    eff = ideal_total / (ms_step * 1e-3)
 
     # dominant kernel by time share
     dom = max(range(nops), key=lambda k: op_ms[k])
@@ -536,18 +548,14 @@ def gpu_arm(args, rank, world, local_rank):
             e2e_step(i)
         e1.record(s_out)
         torch.cuda.synchronize(device)
-        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=device)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(100.0 * ideal_total / (e2e_ms * 1e-3) * world, 3), "unit": UNIT,
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, device)
+        e2e = {"value": job_value(ideal_total, e2e_ms, world), "unit": UNIT,
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h)}
 
     line = {
         "metric": METRIC,
-        "value": round(100.0 * eff * world, 3),
+        "value": job_value(ideal_total, ms_step, world),
         "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
