@@ -236,3 +236,32 @@ def test_attention_rejects_bad_args(T):
         T.mha_fwd(odd, odd, odd)
     assert e.value.status == 3
     assert T.device_error() == 0
+
+
+def test_attention_work_counter_slots_are_reused(T):
+    """Items past the first wave come from a per-launch counter that the last
+    CTA resets: 600 launches (every slot of the counter table taken more than
+    twice, on two streams) must all give the first launch's bits, and that
+    launch the oracle's values."""
+    import torch
+    B, N, Hh, d, mask, window = 2, 1030, 48, 128, O.MASK_CAUSAL_WINDOW, 300
+    q, k, v = _qkv((B, N, Hh, d), (B, N, Hh, d), seed=21)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    first = T.mha_fwd(qd, kd, vd, mask=mask, window=window)
+    ro, _ = O.attention(q[:, None], k[:, None], v[:, None], mask, window)
+    assert_bf16_close(to_f64(first), ro[:, 0], "first launch")
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.empty_like(first) for _ in range(4)]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for n in range(600):
+        with torch.cuda.stream(streams[n & 1]):
+            o = outs[n & 3]
+            o.zero_()
+            T.mha_fwd(qd, kd, vd, mask=mask, window=window, out=o)
+        if n % 50 == 49 or n >= 596:
+            torch.cuda.synchronize()
+            for t in outs:
+                assert torch.equal(t, first), f"launch {n}"
+    torch.cuda.synchronize()
+    assert T.device_error() == 0

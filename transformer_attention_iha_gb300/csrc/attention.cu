@@ -8,10 +8,14 @@
 // scale head_dim ** -0.5, tokens laid out (T outer, units inner)).
 //
 // bf16 path (sm_103a tensor cores), persistent:
-//   One CTA per SM walks a static list of work items; an item is two
-//   adjacent 128-row query tiles of one head.  Items are grouped by heads
-//   (a group's K / V stays in L2 while its items run) and, inside a group,
-//   ordered heaviest first (longest key range), dealt round-robin to CTAs.
+//   One CTA per SM walks a list of work items; an item is two adjacent
+//   128-row query tiles of one head.  Items are grouped by heads (a group's
+//   K / V stays in L2 while its items run) and, inside a group, ordered
+//   heaviest first (longest key range).  CTA b starts on item b and takes
+//   each further item from a global counter when it reaches it (the
+//   producer warp asks one item ahead and passes the index to the other
+//   warps through a four-entry ring in shared memory), so CTAs that draw
+//   short items take more of them.
 //   10 warps:
 //     warps 0-3  softmax + epilogue of query tile 0 (thread = row = TMEM lane)
 //     warps 4-7  softmax + epilogue of query tile 1
@@ -41,6 +45,7 @@ namespace iha {
 namespace {
 
 IHA_DEVICE_ERROR_WORD(attention)
+IHA_WORK_QUEUE(attention)
 
 constexpr int kBM = 128;             // query rows per tile
 constexpr int kBN = 128;             // keys per tile
@@ -51,7 +56,7 @@ constexpr int kKSlots = 2;           // K ring depth (V ring: 2)
 constexpr int kStgBytes = 32 * 128;  // per softmax warp: 32 rows x 64 bf16 of O
 // Q 2x2, K 2x2, V 2x2 chunks | O staging of the 8 softmax warps
 constexpr int kSmemTiles = (4 + 2 * kKSlots + 4) * kTileChunkBytes + 8 * kStgBytes;
-constexpr int kSmemBytes = kSmemTiles + 256 + 1024;  // + barriers + alignment slack
+constexpr int kSmemBytes = kSmemTiles + 512 + 1024;  // + barriers + alignment slack
 constexpr float kRescaleLog2 = 8.0f;
 // L2 budget for the K / V of one head group.
 constexpr int64_t kGroupKVBytes = 48ll << 20;
@@ -66,6 +71,7 @@ struct AttnParams {
   float* lse;
   uint64_t wait_limit_ns;
   int withhold;  // failure-path test: CTA 0 never loads its first V tile
+  int work_slot;  // counter pair of this launch (dynamic item distribution)
 };
 
 struct Item {
@@ -174,8 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto b_pfull = [&](int t) { return bar0 + 8u * (16 + t); };
   auto b_ofull = [&](int t) { return bar0 + 8u * (18 + t); };
   const uint32_t b_drain = bar0 + 8u * 20;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 22);
+  auto b_ifull = [&](int s) { return bar0 + 8u * (22 + s); };   // item ring, 4 entries
+  auto b_iempty = [&](int s) { return bar0 + 8u * (26 + s); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  unsigned int* work = g_work[p.work_slot];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
@@ -196,6 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_ofull(s), 1);
     }
     mbar_init(b_drain, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(b_ifull(s), 1);
+      mbar_init(b_iempty(s), 9);  // the MMA warp and the 8 softmax warps
+    }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -207,6 +221,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Next item index for a consumer warp (whole warp; false once the wait
+  // gave up).  Item indices >= n_items end the walk.
+  uint32_t in_c = 0;  // ring entries consumed by this warp
+  auto next_item = [&](int& idx) -> bool {
+    const int s = (int)(in_c & 3u);
+    if (!mbar_wait_warp(b_ifull(s), (in_c >> 2) & 1u, abort_flag, p.wait_limit_ns)) return false;
+    idx = item_ring[s];
+    __syncwarp();
+    if (elect_one()) mbar_arrive(b_iempty(s));
+    __syncwarp();
+    ++in_c;
+    return true;
+  };
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -255,7 +282,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         return n + 1;
       };
-      for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+      int idx = blockIdx.x;
+      for (uint32_t in = 0; ok; ++in) {
+        // publish the item to the other warps
+        const int s = (int)(in & 3u);
+        if (in >= 4 && !(ok = mbar_wait_warp(b_iempty(s), ((in >> 2) - 1) & 1u, abort_flag, lim)))
+          break;
+        if (elect_one()) {
+          item_ring[s] = idx;
+          mbar_arrive(b_ifull(s));
+        }
+        __syncwarp();
+        if (idx >= p.n_items) break;
+        unsigned int nxt = 0;
+        if (lane == 0) nxt = (unsigned int)work_next(work);  // used after the loads
         const Item it = decode_item(p, idx);
         qn0 = load_q(it, 0, qn0);
         for (int j = it.jlo; ok && j <= it.jhi; ++j) {
@@ -263,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && j == it.jlo && it.act1) qn1 = load_q(it, 1, qn1);
           if (ok) vc = load_kv(it, j, true, vc);
         }
+        idx = (int)__shfl_sync(0xffffffffu, nxt, 0);
       }
       if (!ok) raise_error(abort_flag);
       // Whoever aborted, no copy may still be landing when the CTA exits: wait
@@ -315,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
-      for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+      int idx = 0;
+      while (ok && (ok = next_item(idx)) && idx < p.n_items) {
         const Item it = decode_item(p, idx);
         const uint32_t kbase = kc, vbase = vc;
         uint32_t k_ready = 0;  // K tiles of this item known to be loaded
@@ -401,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t sn = 0, on = 0;  // S tiles consumed, O tiles consumed
     bool ok = true;
-    for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+    int idx = 0;
+    while (ok && (ok = next_item(idx)) && idx < p.n_items) {
       const Item it = decode_item(p, idx);
       if (t == 1 && !it.act1) continue;
       const int qt = it.qt0 + t;
@@ -556,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (threadIdx.x == 0) work_leave(work);
 }
 
 // ---------------------------------------------------------------- fp32 path
@@ -714,6 +758,7 @@ iha_status launch_tc(const void* q, const void* k, const void* v, void* o, float
   p.lse = lse;
   p.wait_limit_ns = wait_limit_for_next_launch();
   p.withhold = withhold_for_this_launch() ? 1 : 0;
+  p.work_slot = (int)attention_work_slot();
   const cudaError_t ae = set_tc_attributes();
   if (ae != cudaSuccess)
     return fail(IHA_ERR_CUDA, "mha_fwd (smem attribute): %s", cudaGetErrorString(ae));

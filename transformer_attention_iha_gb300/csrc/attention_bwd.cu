@@ -15,7 +15,9 @@
 //                         128), and dQ_acc (fp32) zeroed;
 //   attn_bwd_tc_kernel    persistent, one CTA per SM; a work item is one
 //                         128-key tile of one head and loops over the query
-//                         tiles that see it (causal / window block skipping):
+//                         tiles that see it (causal / window block skipping);
+//                         CTA b starts on item b and takes every further item
+//                         from a global counter (longest items first):
 //                           S^T  = K Q^T,  dP^T = V dO^T      (TMEM)
 //                           P^T, dS^T by 4 compute warps (thread = key),
 //                           fp32 P kept over S^T in TMEM for dS
@@ -45,6 +47,7 @@ namespace iha {
 namespace {
 
 IHA_DEVICE_ERROR_WORD(attention_bwd)
+IHA_WORK_QUEUE(attention_bwd)
 
 constexpr int kB = 128;                      // keys (and queries) per tile
 constexpr int kChunkB = kB * 128;            // one 64-wide chunk of a 128-row tile (16 KB)
@@ -57,7 +60,7 @@ constexpr int kCompute = 256;  // threads of warps 0-7
 // a kernel that finds otherwise reports DEV_ERR_SMEM_ALIGN and does nothing.
 constexpr int kSmemTiles = 7 * kTileB;
 constexpr int kLDBytes = 2 * 2 * kB * 4;  // 2 stages x (lse2, D) x 128 floats
-constexpr int kSmemBytes = kSmemTiles + kLDBytes + 256;
+constexpr int kSmemBytes = kSmemTiles + kLDBytes + 512;
 
 struct BwdParams {
   int B, Hh, N, d, Npad, ksteps, nch;
@@ -69,6 +72,7 @@ struct BwdParams {
   float* dq_acc;       // [B, N, Hh, d] fp32
   __nv_bfloat16* dk;   // [B, N, Hh, d]
   __nv_bfloat16* dv;
+  int work_slot;  // counter pair of this launch (dynamic item distribution)
 };
 
 struct Item {
@@ -144,8 +148,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto b_dqempty = [&](int r) { return bar0 + 8u * (14 + r); };
   const uint32_t b_kvout = bar0 + 8u * 16, b_kvoutempty = bar0 + 8u * 17;
   const uint32_t b_drain = bar0 + 8u * 18, b_stg = bar0 + 8u * 19;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  // item ring (4 entries): the producer publishes the index of each item it
+  // starts; the MMA, compute and drain warps take them in order
+  auto b_ifull = [&](int s) { return bar0 + 8u * (20 + s); };
+  auto b_iempty = [&](int s) { return bar0 + 8u * (24 + s); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 28);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  unsigned int* work = g_work[p.work_slot];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t tile_bytes = (uint32_t)p.nch * kChunkB;
@@ -169,6 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_kvoutempty, kCompute);
     mbar_init(b_drain, 1);
     mbar_init(b_stg, 128);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(b_ifull(s), 1);
+      mbar_init(b_iempty(s), 13);  // MMA warp, 8 compute warps, 4 drain warps
+    }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -181,6 +195,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tDK = tmem + 256u, tDV = tmem + 384u;
+  // Next item index for a consumer warp (whole warp; false once the wait
+  // gave up).  Indices >= n_items end the walk.
+  uint32_t in_c = 0;
+  auto next_item = [&](int& idx) -> bool {
+    const int s = (int)(in_c & 3u);
+    if (!mbar_wait_warp(b_ifull(s), (in_c >> 2) & 1u, abort_flag)) return false;
+    idx = item_ring[s];
+    __syncwarp();
+    if (elect_one()) mbar_arrive(b_iempty(s));
+    __syncwarp();
+    ++in_c;
+    return true;
+  };
 
   if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
@@ -191,7 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmDO);
       bool ok = true;
       uint32_t ni = 0, nq = 0;  // items and query tiles loaded
-      for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++ni) {
+      int idx = blockIdx.x;
+      for (;; ++ni) {
+        const int s = (int)(ni & 3u);
+        if (ni >= 4 && !(ok = mbar_wait(b_iempty(s), ((ni >> 2) - 1) & 1u, abort_flag))) break;
+        item_ring[s] = idx;
+        mbar_arrive(b_ifull(s));
+        if (idx >= p.n_items) break;
+        const int nxt = work_next(work);  // used after this item's loads
         const Item it = decode_item(p, idx);
         if (ni > 0 && !(ok = mbar_wait(b_kvempty, (ni - 1) & 1, abort_flag))) break;
         mbar_arrive_expect_tx(b_kvfull, 2 * tile_bytes);
@@ -213,6 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         it.b);
           }
         }
+        if (!ok) break;
+        idx = nxt;
       }
       if (!ok) raise_error(abort_flag);
       // no copy may still be landing when the CTA exits
@@ -230,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_dq = idesc_bf16_f32(128, 128, true, true);        // dQ^T
       bool ok = true;
       uint32_t ni = 0, gt = 0;  // items, query tiles (global count)
-      for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++ni) {
+      int idx = 0;
+      for (; ok && (ok = next_item(idx)) && idx < p.n_items; ++ni) {
         const Item it = decode_item(p, idx);
         if (!(ok = mbar_wait_warp(b_kvfull, ni & 1, abort_flag))) break;
         // dK / dV of the previous item have been read out
@@ -323,7 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hf = warp >> 2;                // query columns 64 hf .. 64 hf + 63
     bool ok = true;
     uint32_t ni = 0, gt = 0;
-    for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x, ++ni) {
+    int idx = 0;
+    for (; ok && (ok = next_item(idx)) && idx < p.n_items; ++ni) {
       const Item it = decode_item(p, idx);
       const int kj = it.jt * kB + row;  // key index
       // queries that see this key: [vis_lo, vis_hi]
@@ -467,7 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool issuer = wq == 0 && lane == 0;
     bool ok = true;
     uint32_t gt = 0;
-    for (int idx = blockIdx.x; ok && idx < p.n_items; idx += gridDim.x) {
+    int idx = 0;
+    while (ok && (ok = next_item(idx)) && idx < p.n_items) {
       const Item it = decode_item(p, idx);
       for (int qt = it.qlo; qt <= it.qhi; ++qt, ++gt) {
         const int r = gt & 1, s = gt & 1;
@@ -511,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (threadIdx.x == 0) work_leave(work);
 }
 
 // D[hb][i] = sum_f dO o O, lse2[hb][i] = lse * log2(e) (zero in the padding),
@@ -653,6 +693,7 @@ iha_status mha_bwd_launch(const void* q, const void* k, const void* v, const voi
   if (g > p.n_hb) g = p.n_hb;
   p.group = (int)g;
   p.n_items = p.n_hb * p.n_kt;
+  p.work_slot = (int)attention_bwd_work_slot();
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse2 = lse2;

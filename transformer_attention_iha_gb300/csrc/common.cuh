@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "iha.h"
 
 namespace iha {
@@ -43,6 +45,21 @@ enum : unsigned { DEV_ERR_KEEP_INDEX = 1u, DEV_ERR_WAIT_TIMEOUT = 2u, DEV_ERR_SM
 // code); its reader is registered here and iha_device_error() ORs them all.
 typedef int (*dev_error_reader)(int clear);
 int register_dev_error_reader(dev_error_reader r);
+
+// Dynamic work distribution for persistent kernels.  Each translation unit
+// that uses it owns a table of kWorkSlots counter pairs {next, done}; every
+// launch takes the next slot (round robin on the host), CTA b starts on item
+// b and takes each further item from the slot's `next` counter (offset by the
+// grid), so a CTA that finishes early takes more of the remaining items.  The
+// last CTA to leave resets the pair for the next launch that takes the slot
+// (launches sharing a slot would need kWorkSlots launches in flight at once).
+constexpr int kWorkSlots = 256;
+#define IHA_WORK_QUEUE(tag)                                                     \
+  static __device__ unsigned int g_work[::iha::kWorkSlots][2];                  \
+  static unsigned int tag##_work_slot() {                                       \
+    static std::atomic<unsigned int> seq{0};                                    \
+    return seq.fetch_add(1u, std::memory_order_relaxed) % ::iha::kWorkSlots;    \
+  }
 
 #define IHA_DEVICE_ERROR_WORD(tag)                                              \
   static __device__ unsigned int g_dev_error;                                   \
@@ -396,6 +413,22 @@ __device__ __forceinline__ void mma_drain_warp(uint32_t bar) {
   mma_commit_warp(bar);
   volatile int no_abort = 0;
   mbar_wait(bar, 0, &no_abort);
+}
+
+// ---- dynamic work distribution (see IHA_WORK_QUEUE)
+// The item after this CTA's current one (one lane asks; items >= the item
+// count mean "no more").
+__device__ __forceinline__ int work_next(unsigned int* slot) {
+  return (int)(atomicAdd(slot, 1u) + gridDim.x);
+}
+// Called by one thread of the CTA after every work_next of the CTA: the last
+// CTA to leave resets the slot for a later launch.
+__device__ __forceinline__ void work_leave(unsigned int* slot) {
+  __threadfence();
+  if (atomicAdd(slot + 1, 1u) == gridDim.x - 1) {
+    atomicExch(slot, 0u);
+    atomicExch(slot + 1, 0u);
+  }
 }
 
 // ---- misc
