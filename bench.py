@@ -102,8 +102,8 @@ def op_table():
     x_b, y_b, w_b = tok * pm.H * pm.d * 2, tok * pm.HP * pm.d * 2, pm.HP * pm.H * 4
     pf = 2 * tok * pm.HP * pm.H * pm.d
     ops.append(("premix_fwd_qkv", 3 * (x_b + y_b + w_b), 3 * pf))
-    for t in "qkv":   # dX and dW from one read of dY and X
-        ops.append((f"premix_bwd_{t}", y_b + 2 * x_b + 2 * w_b, 2 * pf))
+    # dX and dW of Q, K and V in one launch, each from one read of dY and X
+    ops.append(("premix_bwd_qkv", 3 * (y_b + 2 * x_b + 2 * w_b), 3 * 2 * pf))
     aw = S.LLAMA_WINDOW
     attn_fl = 4 * aw.d * _attn_pairs(aw.N, "window", S.WINDOW_KEYS) * aw.HP * aw.B
     tens = aw.B * aw.N * aw.HP * aw.d * 2
@@ -127,10 +127,11 @@ def op_table():
 
 
 def launches_per_step() -> int:
-    # premix fwd (Q, K, V in one launch); premix bwd 3 x (zero dW + kernel);
-    # window attention; its backward (preprocess, kernel, postprocess);
-    # gather, MU attention, scatter; long-context premix (one launch) + attention
-    return 1 + 3 * 2 + 1 + 3 + 3 + 1 + 1
+    # premix fwd (Q, K, V in one launch); premix bwd (zero the three dW + one
+    # kernel for Q, K, V); window attention; its backward (preprocess, kernel,
+    # postprocess); gather, MU attention, scatter; long-context premix (one
+    # launch) + attention
+    return 1 + 2 + 1 + 3 + 3 + 1 + 1
 
 
 def _input_recipes(seed: int):
@@ -158,7 +159,7 @@ def host_inputs(seed: int, keys=None):
 # inputs each op of the step reads (directly or through the op that feeds it)
 OP_INPUTS = {
     "premix_fwd_qkv": [f"{a}_{t}" for t in "qkv" for a in "xw"],
-    **{f"premix_bwd_{t}": [f"dy_{t}", f"x_{t}", f"w_{t}"] for t in "qkv"},
+    "premix_bwd_qkv": [f"{a}_{t}" for t in "qkv" for a in ("dy", "x", "w")],
     "attention_window": ["a_q", "a_k", "a_v"],
     "attention_window_bwd": ["a_q", "a_k", "a_v", "a_do"],
     "mu_gather": ["mu_x", "mu_keep"],
@@ -236,10 +237,10 @@ class Step:
         T.premix_fwd_qkv([i[f"x_{t}"] for t in "qkv"], [i[f"w_{t}"] for t in "qkv"], pm.P,
                          rope=True, rope_base=S.ROPE_BASE, out=tuple(self.y[t] for t in "qkv"))
         done()
-        for t in "qkv":
-            T.premix_bwd(i[f"dy_{t}"], i[f"x_{t}"], i[f"w_{t}"], rope=(t != "v"),
-                         rope_base=S.ROPE_BASE, dx=self.dx[t], dw=self.dw[t])
-            done()
+        T.premix_bwd_qkv([i[f"dy_{t}"] for t in "qkv"], [i[f"x_{t}"] for t in "qkv"],
+                         [i[f"w_{t}"] for t in "qkv"], rope=True, rope_base=S.ROPE_BASE,
+                         dxs=tuple(self.dx[t] for t in "qkv"), dws=tuple(self.dw[t] for t in "qkv"))
+        done()
         T.mha_fwd(i["a_q"], i["a_k"], i["a_v"], mask=T.MASK_CAUSAL_WINDOW, window=S.WINDOW_KEYS,
                   out=self.o, lse=self.lse)
         done()
@@ -706,10 +707,12 @@ def single_op(T, torch, name, dev, device):
         y = tuple(e((pm.B, pm.N, pm.HP, pm.d)) for _ in range(3))
         return lambda: T.premix_fwd_qkv([i[f"x_{u}"] for u in "qkv"], [i[f"w_{u}"] for u in "qkv"],
                                         pm.P, rope=True, rope_base=S.ROPE_BASE, out=y)
-    if kind == "premix_bwd":
-        dx, dw = e((pm.B, pm.N, pm.H, pm.d)), e((pm.H, pm.P, pm.H), torch.float32)
-        return lambda: T.premix_bwd(i[f"dy_{t}"], i[f"x_{t}"], i[f"w_{t}"], rope=(t != "v"),
-                                    rope_base=S.ROPE_BASE, dx=dx, dw=dw)
+    if kind == "premix_bwd_qkv":
+        dx = tuple(e((pm.B, pm.N, pm.H, pm.d)) for _ in range(3))
+        dw = tuple(e((pm.H, pm.P, pm.H), torch.float32) for _ in range(3))
+        return lambda: T.premix_bwd_qkv([i[f"dy_{u}"] for u in "qkv"], [i[f"x_{u}"] for u in "qkv"],
+                                        [i[f"w_{u}"] for u in "qkv"], rope=True,
+                                        rope_base=S.ROPE_BASE, dxs=dx, dws=dw)
     if kind in ("attention_window", "attention_window_bwd"):
         o, lse = e((aw.B, aw.N, aw.HP, aw.d)), e((aw.B, 1, aw.HP, aw.N), torch.float32)
         fwd = lambda: T.mha_fwd(i["a_q"], i["a_k"], i["a_v"], mask=T.MASK_CAUSAL_WINDOW,

@@ -157,6 +157,24 @@ iha_status iha_premix_bwd(const void* dy, const void* x, const float* w, void* d
                           iha_dtype dt, int rope, float rope_base, void* stream);
 
 /*
+ * Premix backward of Q, K and V in one launch ("Pseudo-Token Mixing":
+ * "Backward ... all three Q/K/V in a single launch each", six launches to
+ * two).  Tensor t in (q, k, v) computes exactly what iha_premix_bwd computes
+ * for (dy_t, x_t, w_t) into (dx_t, dw_t); RoPE (when rope != 0) applies to q
+ * and k only.  Every buffer follows iha_premix_bwd's layout and limits; the
+ * three dw are OVERWRITTEN (one small zeroing launch precedes the backward
+ * launch on `stream`); no output may overlap any input or another output.
+ * Shapes outside the tensor-core kernel run as three iha_premix_bwd calls.
+ */
+iha_status iha_premix_bwd_qkv(const void* dyq, const void* dyk, const void* dyv,
+                              const void* xq, const void* xk, const void* xv,
+                              const float* wq, const float* wk, const float* wv,
+                              void* dxq, void* dxk, void* dxv,
+                              float* dwq, float* dwk, float* dwv, int B, int N,
+                              int H, int P, int d, iha_dtype dt, int rope,
+                              float rope_base, void* stream);
+
+/*
  * Multi-head softmax attention forward over Hh heads ("Kernel Design",
  * "FLOP Matching"; MaskUnitAttentionFast.forward):
  *   o[i] = sum_j softmax_j(scale * <q_i, k_j> | visible(i, j)) * v_j

@@ -123,6 +123,60 @@ def test_premix_qkv_fwd_one_launch(T, shape, rope):
     _check_qkv_fwd(T, shape, rope, seed=5 + shape[1])
 
 
+def _check_qkv_bwd(T, shape, rope, seed, base=100.0):
+    """Q, K, V backward in one launch: every tensor's dX and dW against the
+    oracle (inverse RoPE on Q and K only); dX bit-equal to the tensor's own
+    single-tensor backward (dW sums in a different atomic order)."""
+    B, N, H, P, d = shape
+    xs = [S.normal((B, N, H, d), seed, 30 + t) for t in range(3)]
+    dys = [S.normal((B, N, H * P, d), seed, 40 + t) for t in range(3)]
+    ws = [S.premix_weight(H, P, seed, 50 + t) for t in range(3)]
+    dxs, dws = T.premix_bwd_qkv([to_dev(a) for a in dys], [to_dev(a) for a in xs],
+                                [to_dev(a) for a in ws], rope=rope, rope_base=base)
+    for t in range(3):
+        r = rope and t < 2
+        rdx = O.premix_bwd_dx(dys[t], ws[t], rope=r, rope_base=base)
+        assert_bf16_close(to_f64(dxs[t]), rdx, f"qkv dx tensor {t}")
+        rdw = O.premix_bwd_dw(dys[t], xs[t], P, rope=r, rope_base=base)
+        assert_dw_close(to_f64(dws[t]), rdw, dw_abs_sum(dys[t], xs[t], P, r),
+                        dw_chain(B, N, H, P, d, rope=r), r, f"qkv dw tensor {t}")
+        dx1, _ = T.premix_bwd(to_dev(dys[t]), to_dev(xs[t]), to_dev(ws[t]), rope=r,
+                              rope_base=base)
+        assert bool((dx1.view(-1) == dxs[t].view(-1)).all()), f"tensor {t}: dx differs"
+    assert T.device_error() == 0
+
+
+@pytest.mark.parametrize("shape", SHAPES[:3] + TC_EDGE_SHAPES)
+@pytest.mark.parametrize("rope", [False, True])
+def test_premix_qkv_bwd_one_launch(T, shape, rope):
+    if rope and not _rope_ok(shape[4]):
+        pytest.skip("RoPE needs d a power of two")
+    _check_qkv_bwd(T, shape, rope, seed=7 + shape[1])
+
+
+def test_premix_qkv_bwd_llama_shape(T):
+    """B=1, N=8192, H=20, P=4, d=128, RoPE on Q and K, one backward launch:
+    dX on token windows at the start, middle and end, every full dW."""
+    sh = S.LLAMA_PREMIX
+    B, N, H, P, d = sh.B, sh.N, sh.H, sh.P, sh.d
+    xs = [S.normal((B, N, H, d), 4, 30 + t) for t in range(3)]
+    dys = [S.normal((B, N, H * P, d), 4, 40 + t) for t in range(3)]
+    ws = [S.premix_weight(H, P, 4, 50 + t) for t in range(3)]
+    dxs, dws = T.premix_bwd_qkv([to_dev(a) for a in dys], [to_dev(a) for a in xs],
+                                [to_dev(a) for a in ws], rope=True, rope_base=S.ROPE_BASE)
+    for t in range(3):
+        r = t < 2
+        dx = to_f64(dxs[t])
+        for n0 in (0, 4093, N - 131):
+            sl = slice(n0, n0 + 131)
+            rdx = O.premix_bwd_dx(dys[t][:, sl], ws[t], rope=r, rope_base=S.ROPE_BASE, pos0=n0)
+            assert_bf16_close(dx[:, sl], rdx, f"tensor {t} dx@{n0}")
+        rdw = O.premix_bwd_dw(dys[t], xs[t], P, rope=r, rope_base=S.ROPE_BASE)
+        assert_dw_close(to_f64(dws[t]), rdw, dw_abs_sum(dys[t], xs[t], P, r),
+                        dw_chain(B, N, H, P, d, rope=r), r, f"tensor {t} dw full")
+    assert T.device_error() == 0
+
+
 def test_premix_qkv_fwd_f32_tiny_layer(T):
     sh = S.TINY
     _check_qkv_fwd(T, (sh.B, sh.N, sh.H, sh.P, sh.d), True, seed=9, dtype="f32")

@@ -34,7 +34,7 @@ SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_prem
            "mha_fwd", "mu_gather", "mu_scatter", "iha_status_string", "iha_last_error",
            "iha_device_error", "iha_test_fail_next_wait", "mha_bwd", "mha_bwd_workspace_bytes",
            "mha_bwd_noalloc", "iha_premix_fwd_qkv", "mu_attention_fused",
-           "iha_premix_fwd_qkv_interleaved")
+           "iha_premix_fwd_qkv_interleaved", "iha_premix_bwd_qkv")
 
 
 class IHAError(RuntimeError):
@@ -83,10 +83,11 @@ def lib() -> C.CDLL:
     L.mu_gather.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     L.mu_scatter.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     L.mu_attention_fused.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    L.iha_premix_bwd_qkv.argtypes = [vp] * 15 + [i, i, i, i, i, i, i, f, vp]
     for name in ("iha_premix_fwd", "iha_premix_fwd_qkv", "iha_premix_fwd_qkv_interleaved",
                  "iha_premix_bwd_dx",
                  "iha_premix_bwd_dw", "iha_premix_bwd", "mha_fwd", "mha_bwd", "mu_gather",
-                 "mu_scatter", "mu_attention_fused"):
+                 "mu_scatter", "mu_attention_fused", "iha_premix_bwd_qkv"):
         getattr(L, name).restype = C.c_int
     L.iha_status_string.argtypes = [i]
     L.iha_status_string.restype = C.c_char_p
@@ -295,6 +296,42 @@ def premix_bwd(dy, x, w, rope: bool = False, rope_base: float = 10000.0, dx=None
                                _dt(x), int(rope), float(rope_base), _stream(stream)),
           "iha_premix_bwd")
     return dx, dw
+
+
+def premix_bwd_qkv(dys, xs, ws, rope: bool = False, rope_base: float = 10000.0, dxs=None,
+                   dws=None, stream=None):
+    """((dX_q, dX_k, dX_v), (dW_q, dW_k, dW_v)) of the three premixes in one
+    backward launch; inverse RoPE (when rope) on Q and K only."""
+    torch = _torch()
+    if len(dys) != 3 or len(xs) != 3 or len(ws) != 3:
+        raise ValueError("dys, xs and ws must hold three tensors (q, k, v)")
+    x0 = xs[0]
+    _expect(x0, "xq")
+    if x0.dim() != 4:
+        raise ValueError("x must be [B, N, H, d]")
+    B, N, H, d = x0.shape
+    if ws[0].dim() != 3:
+        raise ValueError("w must be [H, P, H]")
+    P = ws[0].shape[1]
+    for t in range(3):
+        _expect(xs[t], f"x[{t}]", (B, N, H, d), x0.dtype, x0.device)
+        _expect(ws[t], f"w[{t}]", (H, P, H), torch.float32, x0.device)
+        _expect(dys[t], f"dy[{t}]", (B, N, H * P, d), x0.dtype, x0.device)
+    if dxs is None:
+        dxs = tuple(torch.empty_like(x0) for _ in range(3))
+    if dws is None:
+        dws = tuple(torch.empty((H, P, H), dtype=torch.float32, device=x0.device)
+                    for _ in range(3))
+    if len(dxs) != 3 or len(dws) != 3:
+        raise ValueError("dxs and dws must hold three tensors")
+    for t in range(3):
+        _expect(dxs[t], f"dx[{t}]", (B, N, H, d), x0.dtype, x0.device)
+        _expect(dws[t], f"dw[{t}]", (H, P, H), torch.float32, x0.device)
+    check(lib().iha_premix_bwd_qkv(*(_ptr(t) for t in dys), *(_ptr(t) for t in xs),
+                                   *(_ptr(t) for t in ws), *(_ptr(t) for t in dxs),
+                                   *(_ptr(t) for t in dws), B, N, H, P, d, _dt(x0), int(rope),
+                                   float(rope_base), _stream(stream)), "iha_premix_bwd_qkv")
+    return tuple(dxs), tuple(dws)
 
 
 # ---------------------------------------------------------------- attention

@@ -431,6 +431,11 @@ __global__ void __launch_bounds__(256) premix_dw_f32_kernel(const float* __restr
 __global__ void zero_f32_kernel(float* p, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0.f;
 }
+// Three buffers of n floats, one block each.
+__global__ void zero3_f32_kernel(float* a, float* b, float* c, int n) {
+  float* p = blockIdx.x == 0 ? a : (blockIdx.x == 1 ? b : c);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) p[i] = 0.f;
+}
 
 // ---------------------------------------------------------------- host side
 iha_status check_common(const char* name, const void* a, const void* b, const void* out, int B,
@@ -725,6 +730,55 @@ iha_status iha_premix_bwd(const void* dy, const void* x, const float* w, void* d
   st = iha_premix_bwd_dx(dy, w, dx, B, N, H, P, d, dt, rope, rope_base, stream);
   if (st != IHA_OK) return st;
   return iha_premix_bwd_dw(dy, x, dw, B, N, H, P, d, dt, rope, rope_base, stream);
+}
+
+iha_status iha_premix_bwd_qkv(const void* dyq, const void* dyk, const void* dyv,
+                              const void* xq, const void* xk, const void* xv, const float* wq,
+                              const float* wk, const float* wv, void* dxq, void* dxk,
+                              void* dxv, float* dwq, float* dwk, float* dwv, int B, int N, int H,
+                              int P, int d, iha_dtype dt, int rope, float rope_base,
+                              void* stream) {
+  using namespace iha;
+  const void* dy[3] = {dyq, dyk, dyv};
+  const void* x[3] = {xq, xk, xv};
+  const float* w[3] = {wq, wk, wv};
+  void* dx[3] = {dxq, dxk, dxv};
+  float* dw[3] = {dwq, dwk, dwv};
+  for (int t = 0; t < 3; ++t) {
+    iha_status st = check_common("iha_premix_bwd_qkv", dy[t], x[t], dx[t], B, N, H, P, d, dt,
+                                 t < 2 ? rope : 0, rope_base);
+    if (st != IHA_OK) return st;
+    if (!w[t] || !dw[t]) return fail(IHA_ERR_INVALID_ARG, "iha_premix_bwd_qkv: null pointer");
+    if (!aligned16(dw[t]))
+      return fail(IHA_ERR_ALIGNMENT, "iha_premix_bwd_qkv: dw must be 16-byte aligned");
+  }
+  const PremixGeom g = make_geom(B, N, H, P, d, rope_base);
+  const size_t es = dt == IHA_BF16 ? 2 : 4;
+  const size_t nx = g.ntok * H * d * es, ny = g.ntok * g.HP * d * es, nw = (size_t)g.HP * H * 4;
+  for (int t = 0; t < 3; ++t)
+    for (int u = 0; u < 3; ++u) {
+      const bool clash =
+          overlaps(dx[t], nx, dy[u], ny) || overlaps(dx[t], nx, x[u], nx) ||
+          overlaps(dx[t], nx, w[u], nw) || overlaps(dw[t], nw, dy[u], ny) ||
+          overlaps(dw[t], nw, x[u], nx) || overlaps(dw[t], nw, w[u], nw) ||
+          overlaps(dw[t], nw, dx[u], nx) ||
+          (u != t && (overlaps(dx[t], nx, dx[u], nx) || overlaps(dw[t], nw, dw[u], nw)));
+      if (clash)
+        return fail(IHA_ERR_INVALID_ARG, "iha_premix_bwd_qkv: an output overlaps another buffer");
+    }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == IHA_BF16 && premix_bwd_tc_supported(H, P, d, true, true, rope != 0)) {
+    zero3_f32_kernel<<<3, 256, 0, s>>>(dw[0], dw[1], dw[2], g.HP * H);
+    const iha_status st = check_launch("iha_premix_bwd_qkv (zero dw)");
+    if (st != IHA_OK) return st;
+    return premix_bwd_tc_multi(3, dy, x, w, dx, dw, B, N, H, P, d, rope ? 3 : 0, rope_base, s);
+  }
+  for (int t = 0; t < 3; ++t) {
+    const iha_status st = iha_premix_bwd(dy[t], x[t], w[t], dx[t], dw[t], B, N, H, P, d, dt,
+                                         t < 2 ? rope : 0, rope_base, stream);
+    if (st != IHA_OK) return st;
+  }
+  return IHA_OK;
 }
 
 }  // extern "C"

@@ -32,6 +32,8 @@
 // A operand, written once per CTA.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "premix_tc.h"
 
@@ -420,9 +422,17 @@ iha_status premix_fwd_tc_multi(int ntens, const void* const* x, const float* con
   const size_t smem = fixed + (size_t)p.x_stages * p.stage_bytes;
   if (smem > 227 * 1024) return fail(IHA_ERR_UNSUPPORTED, "premix forward: shared memory budget");
   auto kern = d == 128 ? premix_fwd_tc_kernel<128> : premix_fwd_tc_kernel<64>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return check_launch("premix forward (smem attribute)");
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {  // both instantiations, once per process
+    attr_err = cudaFuncSetAttribute(premix_fwd_tc_kernel<128>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(premix_fwd_tc_kernel<64>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(IHA_ERR_CUDA, "premix forward (smem attribute): %s", cudaGetErrorString(attr_err));
   int grid = sm_count();
   if (grid > ntens * p.n_stages) grid = ntens * p.n_stages;
   kern<<<grid, kThreads, smem, stream>>>(maps, p);
@@ -483,9 +493,13 @@ constexpr int kBwdNA = 6;  // dX accumulator slots of 64 TMEM columns
 // tensor-core accumulation drift systematically (measured 3e-5 relative at
 // 216 tokens per CTA); chunks of 8 tokens keep it near fp32 rounding.
 constexpr int kDwChunk = 8;
+// Largest dynamic shared memory of a backward launch: the per-block limit
+// less room for the kernel's static shared words.
+constexpr int kBwdSmemMax = 227 * 1024 - 64;
 
 struct BwdParams {
   int ntok, N, H, HP, hp_pad, nkb, ns;
+  int ntens, rope_mask;  // tensors of the launch; bit t: tensor t takes RoPE
   uint32_t chunk;        // one 64-feature dY box: hp_pad x 128 B
   uint32_t dy_bytes;     // dY bytes per stage (2 boxes)
   uint32_t x_bytes;      // X bytes per token (2 boxes of 64 x 32), 0 without dW
@@ -495,19 +509,21 @@ struct BwdParams {
   RopeTable rt;
 };
 
+// One tensor's backward by the whole CTA (every thread calls it): its own
+// barriers, W^T tile and pipeline in the 1024-aligned dynamic shared memory
+// `smem`, TMEM allocated by the caller; the barriers are invalidated at the
+// end so that the next pass may reuse the memory.
 template <bool DO_DX, bool DO_DW, bool ROPE>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    premix_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmDY,
-                         const __grid_constant__ CUtensorMap tmX,
-                         const __grid_constant__ CUtensorMap tmDX, const float* __restrict__ w,
-                         float* __restrict__ dw, const BwdParams p) {
+__device__ __forceinline__ void premix_bwd_pass(const CUtensorMap& tmDY, const CUtensorMap& tmX,
+                                                const CUtensorMap& tmDX,
+                                                const float* __restrict__ w,
+                                                float* __restrict__ dw, const BwdParams& p,
+                                                uint8_t* smem, const uint32_t tmem,
+                                                volatile int* abort_flag) {
   constexpr int D = 128;
   constexpr bool PREP = ROPE && DO_DW;   // R X (hi / lo) for the dW MMA
   constexpr bool EXCH = ROPE && DO_DX;   // warp-pair exchange for the inverse rotation
   constexpr int NDW = PREP ? 64 : 32;    // dW accumulator columns
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   // layout: W^T (nkb blocks of 64 rows x 128 B) | stages | R X (2 slots x 2 boxes
   //         of 64 rows) | dX staging (8 warps x 2) | exchange (8 warps x 2) |
   //         rope table (64 float2) | barriers
@@ -535,8 +551,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto b_dwfull = [&](int b) { return bar0 + 8u * (2 * NS + 20 + b); };
   auto b_dwempty = [&](int b) { return bar0 + 8u * (2 * NS + 22 + b); };
   const uint32_t b_drain = bar0 + 8u * (2 * NS + 24);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NS + 25);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_my = (p.ntok - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -559,7 +573,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(b_dwempty(b), 128);
     }
     mbar_init(b_drain, 1);
-    *abort_flag = 0;
     mbar_init_fence();
   }
   if (DO_DX && tid < 256) {
@@ -597,14 +610,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   }
   fence_proxy_async_smem();
-  if (warp == 9) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_dw = tmem + (uint32_t)(kBwdNA * 64);  // + 64 * buffer
 
   if (warp == 8) {
@@ -878,6 +886,68 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) {  // this pass's barriers are dead; their memory may be reused
+    for (int s = 0; s < NS; ++s) {
+      mbar_inval(b_infull(s));
+      mbar_inval(b_inempty(s));
+    }
+    for (int a = 0; a < kBwdNA; ++a) {
+      mbar_inval(b_accfull(a));
+      mbar_inval(b_accempty(a));
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_inval(b_xrfull(s));
+      mbar_inval(b_xrempty(s));
+      mbar_inval(b_dwfull(s));
+      mbar_inval(b_dwempty(s));
+    }
+    mbar_inval(b_drain);
+  }
+  __syncthreads();
+}
+
+struct BwdMaps {
+  CUtensorMap dy[kMaxTens], x[kMaxTens], dx[kMaxTens];
+};
+struct BwdPtrs {
+  const float* w[kMaxTens];
+  float* dw[kMaxTens];
+};
+
+// The backward of p.ntens tensors (Q, K, V: each its own dY, X, W, dX, dW)
+// in one launch: every CTA runs one pass per tensor over its share of the
+// tokens, the RoPE variant chosen per tensor (bit t of p.rope_mask).  TMEM
+// is allocated once for all passes; a raised abort flag skips the rest.
+template <bool DO_DX, bool DO_DW>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    premix_bwd_tc_kernel(const __grid_constant__ BwdMaps maps, const BwdPtrs ptrs,
+                         const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  volatile int* abort_flag = &s_abort;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) *abort_flag = 0;
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  for (int t = 0; t < p.ntens && *abort_flag == 0; ++t) {
+    if ((p.rope_mask >> t) & 1)
+      premix_bwd_pass<DO_DX, DO_DW, true>(maps.dy[t], maps.x[t], maps.dx[t], ptrs.w[t],
+                                          ptrs.dw[t], p, smem, tmem, abort_flag);
+    else
+      premix_bwd_pass<DO_DX, DO_DW, false>(maps.dy[t], maps.x[t], maps.dx[t], ptrs.w[t],
+                                           ptrs.dw[t], p, smem, tmem, abort_flag);
+  }
+  tc_fence_before();
+  __syncthreads();
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -910,7 +980,7 @@ bool bwd_geometry(int H, int P, bool do_dx, bool do_dw, bool rope, BwdParams* p,
   const size_t fixed = 1024 + (do_dx ? (size_t)p->nkb * 8192u : 0) + (prep ? 32768 : 0) +
                        (do_dx ? 16u * p->out_bytes : 0) + (exch ? 16u * p->ex_bytes : 0) +
                        (prep ? 1024 : 0) + 512;  // last: barriers (<= 2*4 + 25 slots)
-  const size_t limit = 227 * 1024;
+  const size_t limit = kBwdSmemMax;
   p->ns = 4;
   while (p->ns > 2 && fixed + (size_t)p->ns * p->stage_bytes > limit) --p->ns;
   *smem = fixed + (size_t)p->ns * p->stage_bytes;
@@ -926,60 +996,113 @@ bool premix_bwd_tc_supported(int H, int P, int d, bool do_dx, bool do_dw, bool r
   return bwd_geometry(H, P, do_dx, do_dw, rope, &p, &smem);
 }
 
-iha_status premix_bwd_tc(const void* dy, const void* x, const float* w, void* dx, float* dw,
-                         int B, int N, int H, int P, int d, int rope, float rope_base,
-                         cudaStream_t stream) {
-  const bool do_dx = dx != nullptr, do_dw = dw != nullptr;
+namespace {
+
+// Dynamic shared memory attribute of each backward instantiation, set once
+// per process (thread-safe) to the largest size any launch asks for.
+template <bool DX, bool DW>
+cudaError_t bwd_smem_attribute() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(premix_bwd_tc_kernel<DX, DW>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemMax);
+  });
+  return err;
+}
+
+}  // namespace
+
+iha_status premix_bwd_tc_multi(int ntens, const void* const* dy, const void* const* x,
+                               const float* const* w, void* const* dx, float* const* dw, int B,
+                               int N, int H, int P, int d, int rope_mask, float rope_base,
+                               cudaStream_t stream) {
+  if (ntens < 1 || ntens > kMaxTens)
+    return fail(IHA_ERR_INVALID_ARG, "premix backward: 1 to 3 tensors per launch");
+  const bool do_dx = dx[0] != nullptr, do_dw = dw[0] != nullptr;
+  for (int t = 1; t < ntens; ++t)
+    if ((dx[t] != nullptr) != do_dx || (dw[t] != nullptr) != do_dw)
+      return fail(IHA_ERR_INVALID_ARG, "premix backward: every tensor needs the same outputs");
+  rope_mask &= (1 << ntens) - 1;
   BwdParams p;
   size_t smem;
-  if (!bwd_geometry(H, P, do_dx, do_dw, rope != 0, &p, &smem))
+  if (!bwd_geometry(H, P, do_dx, do_dw, rope_mask != 0, &p, &smem))
     return fail(IHA_ERR_UNSUPPORTED, "premix backward: shared memory budget");
   p.ntok = B * N;
   p.N = N;
+  p.ntens = ntens;
+  p.rope_mask = rope_mask;
   make_rope_table(&p.rt, d, rope_base);
 
-  CUtensorMap mdy, mx, mdx;
-  {
-    uint64_t dims[3] = {(uint64_t)d, (uint64_t)p.HP, (uint64_t)p.ntok};
-    uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)p.HP * d * 2};
-    uint32_t box[3] = {64, (uint32_t)p.hp_pad, 1};
-    if (encode_tiled(&mdy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(dy), dims, st,
-                     box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return fail(IHA_ERR_CUDA, "premix backward: dY tensor map encoding failed");
+  BwdMaps maps;
+  BwdPtrs ptrs;
+  for (int t = 0; t < ntens; ++t) {
+    ptrs.w[t] = w[t];
+    ptrs.dw[t] = dw[t];
+    {
+      uint64_t dims[3] = {(uint64_t)d, (uint64_t)p.HP, (uint64_t)p.ntok};
+      uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)p.HP * d * 2};
+      uint32_t box[3] = {64, (uint32_t)p.hp_pad, 1};
+      if (encode_tiled(&maps.dy[t], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(dy[t]),
+                       dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return fail(IHA_ERR_CUDA, "premix backward: dY tensor map encoding failed");
+    }
+    maps.x[t] = maps.dy[t];
+    if (do_dw) {
+      uint64_t dims[3] = {(uint64_t)d, (uint64_t)H, (uint64_t)p.ntok};
+      uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)H * d * 2};
+      uint32_t box[3] = {64, 32, 1};
+      if (encode_tiled(&maps.x[t], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x[t]),
+                       dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return fail(IHA_ERR_CUDA, "premix backward: X tensor map encoding failed");
+    }
+    maps.dx[t] = maps.dy[t];
+    if (do_dx) {
+      uint64_t dims[3] = {(uint64_t)d, (uint64_t)H, (uint64_t)p.ntok};
+      uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)H * d * 2};
+      uint32_t box[3] = {32, (uint32_t)H, 1};
+      if (encode_tiled(&maps.dx[t], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dx[t], dims, st, box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return fail(IHA_ERR_CUDA, "premix backward: dX tensor map encoding failed");
+    }
   }
-  mx = mdy;
-  if (do_dw) {
-    uint64_t dims[3] = {(uint64_t)d, (uint64_t)H, (uint64_t)p.ntok};
-    uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)H * d * 2};
-    uint32_t box[3] = {64, 32, 1};
-    if (encode_tiled(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, st, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return fail(IHA_ERR_CUDA, "premix backward: X tensor map encoding failed");
+  for (int t = ntens; t < kMaxTens; ++t) {  // unused slots: valid copies, never read
+    maps.dy[t] = maps.dy[0];
+    maps.x[t] = maps.x[0];
+    maps.dx[t] = maps.dx[0];
+    ptrs.w[t] = nullptr;
+    ptrs.dw[t] = nullptr;
   }
-  mdx = mdy;
-  if (do_dx) {
-    uint64_t dims[3] = {(uint64_t)d, (uint64_t)H, (uint64_t)p.ntok};
-    uint64_t st[2] = {(uint64_t)d * 2, (uint64_t)H * d * 2};
-    uint32_t box[3] = {32, (uint32_t)H, 1};
-    if (encode_tiled(&mdx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dx, dims, st, box,
-                     CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
-      return fail(IHA_ERR_CUDA, "premix backward: dX tensor map encoding failed");
+  void (*kern)(const BwdMaps, const BwdPtrs, const BwdParams);
+  cudaError_t ae;
+  if (do_dx && do_dw) {
+    kern = premix_bwd_tc_kernel<true, true>;
+    ae = bwd_smem_attribute<true, true>();
+  } else if (do_dx) {
+    kern = premix_bwd_tc_kernel<true, false>;
+    ae = bwd_smem_attribute<true, false>();
+  } else {
+    kern = premix_bwd_tc_kernel<false, true>;
+    ae = bwd_smem_attribute<false, true>();
   }
-  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const float*, float*,
-               const BwdParams);
-  if (do_dx && do_dw)
-    kern = rope ? premix_bwd_tc_kernel<true, true, true> : premix_bwd_tc_kernel<true, true, false>;
-  else if (do_dx)
-    kern = rope ? premix_bwd_tc_kernel<true, false, true> : premix_bwd_tc_kernel<true, false, false>;
-  else
-    kern = rope ? premix_bwd_tc_kernel<false, true, true> : premix_bwd_tc_kernel<false, true, false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return check_launch("premix backward (smem attribute)");
+  if (ae != cudaSuccess)
+    return fail(IHA_ERR_CUDA, "premix backward (smem attribute): %s", cudaGetErrorString(ae));
   int grid = sm_count();
   if (grid > p.ntok) grid = p.ntok;
-  kern<<<grid, kBwdThreads, smem, stream>>>(mdy, mx, mdx, w, dw, p);
+  kern<<<grid, kBwdThreads, smem, stream>>>(maps, ptrs, p);
   return check_launch("premix backward");
+}
+
+iha_status premix_bwd_tc(const void* dy, const void* x, const float* w, void* dx, float* dw,
+                         int B, int N, int H, int P, int d, int rope, float rope_base,
+                         cudaStream_t stream) {
+  const void* dys[1] = {dy};
+  const void* xs[1] = {x};
+  const float* ws[1] = {w};
+  void* dxs[1] = {dx};
+  float* dws[1] = {dw};
+  return premix_bwd_tc_multi(1, dys, xs, ws, dxs, dws, B, N, H, P, d, rope ? 1 : 0, rope_base,
+                             stream);
 }
 
 }  // namespace iha

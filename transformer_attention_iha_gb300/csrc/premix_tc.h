@@ -30,6 +30,14 @@ iha_status premix_bwd_tc(const void* dy, const void* x, const float* w, void* dx
                          int B, int N, int H, int P, int d, int rope, float rope_base,
                          cudaStream_t stream);
 
+// The same over ntens (1..3) tensors in one launch: tensor t reads dy[t],
+// x[t], w[t] and writes dx[t] / dw[t] (all dx null or all non-null, the same
+// for dw), rotated when bit t of rope_mask is set; every dw[t] zeroed first.
+iha_status premix_bwd_tc_multi(int ntens, const void* const* dy, const void* const* x,
+                               const float* const* w, void* const* dx, float* const* dw, int B,
+                               int N, int H, int P, int d, int rope_mask, float rope_base,
+                               cudaStream_t stream);
+
 iha_status premix_fwd_tc(const void* x, const float* w, void* y, int B, int N, int H, int P,
                          int d, int rope, float rope_base, cudaStream_t stream);
 
