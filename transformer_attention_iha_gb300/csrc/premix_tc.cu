@@ -475,17 +475,21 @@ namespace iha {
 // Inverse RoPE on dX pairs feature f with f ^ 64, held by warp e ^ 2 of the
 // same group: the pair of warps swaps fp32 values through shared memory
 // (double-buffered, one 64-thread named barrier per token).
-// Roles (384 threads, persistent over tokens):
-//   warps 0-7   dX epilogue: warp e reads features 32*(e%4).. of the CTA's
-//               tokens k with k % 2 == e / 4, stages bf16 [H][32] and
-//               TMA-stores it itself.
-//   warp 8      TMA producer (dY and X tiles, ring of up to 4 stages)
-//   warp 9      MMA issuer and TMEM owner
-//   warps 10-11 R X (hi / lo) for the dW MMA when RoPE is on
+// Roles (320 threads, persistent over tokens):
+//   warps 0-7   token groups: group G = warps 4G..4G+3 takes the CTA's tokens
+//               k with k % 2 == G.  Per token: with RoPE, the token's cos /
+//               sin table (one entry per feature pair, shared by both uses)
+//               and R X (hi / lo) for the dW MMA into the group's own R X
+//               slot; then the dX epilogue: warp e reads features 32*(e%4)..
+//               from TMEM, stages bf16 [H][32] and TMA-stores it itself.
+//               At the start they also build the W^T tile (while the first
+//               tiles load), and group 0 folds the dW partials.
+//   warp  8     TMA producer (dY and X tiles, ring of up to 4 stages)
+//   warp  9     MMA issuer and TMEM owner
 // ===========================================================================
 namespace {
 
-constexpr int kBwdThreads = 384;
+constexpr int kBwdThreads = 320;
 constexpr int kBwdNA = 6;  // dX accumulator slots of 64 TMEM columns
 // dW partials: the tensor core accumulates at most this many tokens (d/16
 // MMA K-steps each) into one of two 64-column TMEM buffers; the partial is
@@ -537,7 +541,8 @@ __device__ __forceinline__ void premix_bwd_pass(const CUtensorMap& tmDY, const C
   const uint32_t sEx = sOut + out_total;
   const uint32_t ex_total = EXCH ? 16u * p.ex_bytes : 0u;
   const uint32_t sRope = sEx + ex_total;
-  const uint32_t rope_bytes = PREP ? 2u * 32u * 16u : 0u;  // 2 tokens x [32] float4
+  // cos / sin tables: [group][buffer][32] float4
+  const uint32_t rope_bytes = (PREP || EXCH) ? 2u * 2u * 32u * 16u : 0u;
   auto gen = [&](uint32_t a) { return smem + (a - sWT); };  // shared address -> pointer
   uint64_t* bars = reinterpret_cast<uint64_t*>(gen((sRope + rope_bytes + 7u) & ~7u));
   const uint32_t bar0 = smem_u32(bars);
@@ -551,6 +556,7 @@ __device__ __forceinline__ void premix_bwd_pass(const CUtensorMap& tmDY, const C
   auto b_dwfull = [&](int b) { return bar0 + 8u * (2 * NS + 20 + b); };
   auto b_dwempty = [&](int b) { return bar0 + 8u * (2 * NS + 22 + b); };
   const uint32_t b_drain = bar0 + 8u * (2 * NS + 24);
+  const uint32_t b_wt = bar0 + 8u * (2 * NS + 25);  // W^T tile built (256 arrivals)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_my = (p.ntok - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -558,14 +564,14 @@ __device__ __forceinline__ void premix_bwd_pass(const CUtensorMap& tmDY, const C
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(b_infull(s), 1);
-      mbar_init(b_inempty(s), 1 + (PREP ? 64 : 0));
+      mbar_init(b_inempty(s), 1 + (PREP ? 128 : 0));
     }
     for (int a = 0; a < kBwdNA; ++a) {
       mbar_init(b_accfull(a), 1);
       mbar_init(b_accempty(a), 128);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(b_xrfull(s), 64);
+      mbar_init(b_xrfull(s), 128);
       mbar_init(b_xrempty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -573,41 +579,8 @@ __device__ __forceinline__ void premix_bwd_pass(const CUtensorMap& tmDY, const C
       mbar_init(b_dwempty(b), 128);
     }
     mbar_init(b_drain, 1);
+    mbar_init(b_wt, 256);
     mbar_init_fence();
-  }
-  if (DO_DX && tid < 256) {
-    // B operand of dX: row n = part * 32 + s (part 0 = bf16 hi, 1 = lo of
-    // W[hp][s]), K = pseudo-head in blocks of 64, 128-byte swizzle.
-    const int nchunks = p.nkb * 64 * 8;
-    for (int idx = tid; idx < nchunks; idx += 256) {
-      const int j = idx & 7, n = (idx >> 3) & 63, blk = idx >> 9;
-      const int part = n >> 5, s = n & 31;
-      const int hp0 = blk * 64 + 8 * j;
-      uint32_t v[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float two[2];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int hp = hp0 + 2 * e + h2;
-          const float wv = (hp < p.HP && s < p.H) ? __ldg(w + hp * p.H + s) : 0.f;
-          const float hi = __bfloat162float(__float2bfloat16_rn(wv));
-          two[h2] = part ? (wv - hi) : hi;
-        }
-        v[e] = pack_bf16x2(two[0], two[1]);
-      }
-      *reinterpret_cast<uint4*>(gen(sWT + (uint32_t)blk * 8192u + (uint32_t)n * 128u +
-                                    (uint32_t)((j ^ (n & 7)) << 4))) =
-          make_uint4(v[0], v[1], v[2], v[3]);
-    }
-  }
-  if (PREP && tid < 256) {  // rows s >= H of both halves of R X stay zero
-    for (int idx = tid; idx < 2 * 2 * 64 * 8; idx += 256) {
-      const int j = idx & 7, n = (idx >> 3) & 63, box = idx >> 9;  // box: slot*2 + chunk
-      if ((n & 31) >= p.H)
-        *reinterpret_cast<uint4*>(gen(sXr + (uint32_t)box * 8192u + (uint32_t)n * 128u +
-                                      (uint32_t)(j << 4))) = make_uint4(0, 0, 0, 0);
-    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -666,6 +639,7 @@ __device__ __forceinline__ void premix_bwd_pass(const CUtensorMap& tmDY, const C
         tc_fence_after();
         if (DO_DX) {
           const int a = k % kBwdNA;
+          if (k == 0 && !(ok = mbar_wait_warp(b_wt, 0, abort_flag))) break;  // W^T built
           if (!(ok = mbar_wait_warp(b_accempty(a), ((k / kBwdNA) & 1) ^ 1, abort_flag))) break;
           tc_fence_after();
           const uint32_t dxd = tmem + (uint32_t)(a * 64);
@@ -714,71 +688,59 @@ __device__ __forceinline__ void premix_bwd_pass(const CUtensorMap& tmDY, const C
       if (!ok) raise_error(abort_flag);
       mma_drain_warp(b_drain);  // no MMA in flight when TMEM is released
     }
-  } else if (warp >= 10) {
-    // ------------------------------------------------------------ R X (hi / lo)
-    if (PREP) {
-      const int u = tid - 320;  // 0..63
-      // cos / sin of the token, double-buffered: [32] x (c_2m, c_2m+1, s_2m, s_2m+1)
-      float* tabs = reinterpret_cast<float*>(gen(sRope));
-      const float2 inv = rope_inv_freq(p.rt, u);
-      for (int k = 0; k < n_my; ++k) {
-        const int tok = blockIdx.x + k * gridDim.x, s = k % NS;
-        const uint32_t xs = sStages + (uint32_t)s * p.stage_bytes + p.dy_bytes;
-        const uint32_t xr = sXr + (uint32_t)(k & 1) * 16384u;
-        float* tw = tabs + (k & 1) * 128;
-        {
-          float c, sn;
-          rope_cos_sin(tok % p.N, inv.x, inv.y, c, sn);
-          tw[4 * (u >> 1) + (u & 1)] = c;
-          tw[4 * (u >> 1) + 2 + (u & 1)] = sn;
-        }
-        // the table is complete (and buffer k & 1 was last read two tokens ago)
-        named_bar_sync(1, 64);
-        if (!mbar_wait(b_infull(s), (k / NS) & 1, abort_flag)) raise_error(abort_flag);
-        if (!mbar_wait(b_xrempty(k & 1), ((k >> 1) & 1) ^ 1, abort_flag)) raise_error(abort_flag);
-        const float4* t4 = reinterpret_cast<const float4*>(tw);
-        for (int task = u; task < p.H * 8; task += 64) {
-          const int j = task / p.H, row = task - j * p.H;  // neighbours share j: table broadcast
-          const uint32_t off = (uint32_t)row * 128u + (uint32_t)((j ^ (row & 7)) << 4);
-          const uint32_t offl = (uint32_t)(row + 32) * 128u + (uint32_t)((j ^ (row & 7)) << 4);
-          const uint4 a = *reinterpret_cast<const uint4*>(gen(xs + off));
-          const uint4 b = *reinterpret_cast<const uint4*>(gen(xs + 4096u + off));
-          const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-          uint32_t ah[4], al[4], bh[4], bl[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            // features 8j + 2e, +1 (x0) and their partners 64 + 8j + 2e, +1 (x1)
-            const float4 cs = t4[4 * j + e];
-            const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
-            const float2 x0 = make_float2(bf16lo_to_f32(av[e]), bf16hi_to_f32(av[e]));
-            const float2 x1 = make_float2(bf16lo_to_f32(bv[e]), bf16hi_to_f32(bv[e]));
-            const float2 ra = __ffma2_rn(x0, c2, __fmul2_rn(make_float2(-x1.x, -x1.y), s2));
-            const float2 rb = __ffma2_rn(x0, s2, __fmul2_rn(x1, c2));
-            ah[e] = pack_bf16x2(ra.x, ra.y);
-            bh[e] = pack_bf16x2(rb.x, rb.y);
-            al[e] = pack_bf16x2(ra.x - bf16lo_to_f32(ah[e]), ra.y - bf16hi_to_f32(ah[e]));
-            bl[e] = pack_bf16x2(rb.x - bf16lo_to_f32(bh[e]), rb.y - bf16hi_to_f32(bh[e]));
-          }
-          // box c of a slot: 64 rows (hi rows 0..31, lo rows 32..63) x 128 B
-          *reinterpret_cast<uint4*>(gen(xr + off)) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
-          *reinterpret_cast<uint4*>(gen(xr + 8192u + off)) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
-          *reinterpret_cast<uint4*>(gen(xr + offl)) = make_uint4(al[0], al[1], al[2], al[3]);
-          *reinterpret_cast<uint4*>(gen(xr + 8192u + offl)) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(b_xrfull(k & 1));
-        mbar_arrive(b_inempty(s));
-      }
-    }
   } else {
-    // ------------------------------------------------------------ dX epilogue
-    // Warp e: features f = 32*(e%4) + lane of the tokens k with k % 2 == e / 4.
-    // Warps 0-3 also fold each dW chunk (TMEM lanes = pseudo-head rows f) into
-    // fp32 registers and add them to dw at the end.
-    const int G = warp >> 2, q = warp & 3;
+    // ------------------------------------------------------------ token groups
+    // Group G (warps 4G..4G+3) takes tokens k with k % 2 == G; warp e holds
+    // features f = 32*(e%4) + lane of them (TMEM lanes of the dX tile).
+    // Group 0 also folds each dW chunk (TMEM lanes = pseudo-head rows f) into
+    // fp32 registers and adds them to dw at the end.
+    const int G = warp >> 2, q = warp & 3, gt = tid & 127;
     const int f = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     const uint32_t wout = sOut + (uint32_t)(warp * 2) * p.out_bytes;
+    if (DO_DX) {
+      // W^T, the B operand of dX, built while the first tiles load: W (fp32)
+      // read once, coalesced, into the not yet used dX staging; then row
+      // n = part * 32 + s (part 0 = bf16 hi, 1 = lo of W[hp][s]), K =
+      // pseudo-head in blocks of 64, 128-byte swizzle.
+      float* wst = reinterpret_cast<float*>(gen(sOut));
+      for (int i = tid; i < p.HP * p.H; i += 256) wst[i] = __ldg(w + i);
+      named_bar_sync(1, 256);
+      const int nchunks = p.nkb * 64 * 8;
+      for (int idx = tid; idx < nchunks; idx += 256) {
+        const int j = idx & 7, n = (idx >> 3) & 63, blk = idx >> 9;
+        const int part = n >> 5, sr = n & 31;
+        const int hp0 = blk * 64 + 8 * j;
+        uint32_t v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float two[2];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int hp = hp0 + 2 * e + h2;
+            const float wv = (hp < p.HP && sr < p.H) ? wst[hp * p.H + sr] : 0.f;
+            const float hi = __bfloat162float(__float2bfloat16_rn(wv));
+            two[h2] = part ? (wv - hi) : hi;
+          }
+          v[e] = pack_bf16x2(two[0], two[1]);
+        }
+        *reinterpret_cast<uint4*>(gen(sWT + (uint32_t)blk * 8192u + (uint32_t)n * 128u +
+                                      (uint32_t)((j ^ (n & 7)) << 4))) =
+            make_uint4(v[0], v[1], v[2], v[3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(b_wt);
+      named_bar_sync(1, 256);  // the staging is free again
+    }
+    const uint32_t xr = sXr + (uint32_t)G * 16384u;  // this group's R X slot
+    if (PREP) {  // its rows s >= H stay zero
+      for (int idx = gt; idx < 2 * 64 * 8; idx += 128) {
+        const int j = idx & 7, n = (idx >> 3) & 63, c = idx >> 9;
+        if ((n & 31) >= p.H)
+          *reinterpret_cast<uint4*>(gen(xr + (uint32_t)c * 8192u + (uint32_t)n * 128u +
+                                        (uint32_t)(j << 4))) = make_uint4(0, 0, 0, 0);
+      }
+    }
     float dwacc[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) dwacc[e] = 0.f;
@@ -804,74 +766,139 @@ __device__ __forceinline__ void premix_bwd_pass(const CUtensorMap& tmDY, const C
       tc_fence_before();
       mbar_arrive(b_dwempty(b));
     };
-    const float2 inv = ROPE ? rope_inv_freq(p.rt, f & 63) : make_float2(0.f, 0.f);
+    // cos / sin tables [group][buffer]: 32 float4 (c_2m, c_2m+1, s_2m, s_2m+1)
+    float* tabs = reinterpret_cast<float*>(gen(sRope));
+    const float2 inv = ROPE ? rope_inv_freq(p.rt, gt & 63) : make_float2(0.f, 0.f);
     const int n_dwc = (n_my + kDwChunk - 1) / kDwChunk;
     int dwc_done = 0;
     int it = 0;
-    if (DO_DX) {
-      // After an abort the loop keeps stepping (TMEM and stores skipped) so
-      // that the two warps of an inverse-RoPE pair still meet at every named
-      // barrier; every later wait returns at once on the raised flag.
+    if (DO_DX || PREP) {
+      // After an abort the loop keeps stepping (TMEM, shared-memory work and
+      // stores skipped) so that every warp still meets the group's and the
+      // inverse-RoPE pair's named barriers; later waits return at once.
       for (int k = G; k < n_my; k += 2, ++it) {
-        const int tok = blockIdx.x + k * gridDim.x;
-        const int a = k % kBwdNA;
-        float c = 1.f, sn = 0.f;
-        if (ROPE) rope_cos_sin(tok % p.N, inv.x, inv.y, c, sn);
-        const bool live = ok && mbar_wait_warp(b_accfull(a), (k / kBwdNA) & 1, abort_flag);
-        if (ok && !live) {
-          ok = false;
-          raise_error(abort_flag);
+        const int tok = blockIdx.x + k * gridDim.x, s = k % NS;
+        const float* tw = tabs + (G * 2 + (it & 1)) * 128;
+        if (ROPE) {
+          if (gt < 64) {
+            float c, sn;
+            rope_cos_sin(tok % p.N, inv.x, inv.y, c, sn);
+            float* twm = tabs + (G * 2 + (it & 1)) * 128;
+            twm[4 * (gt >> 1) + (gt & 1)] = c;
+            twm[4 * (gt >> 1) + 2 + (gt & 1)] = sn;
+          }
+          named_bar_sync(6 + G, 128);  // the table is complete
         }
-        float v[32];
-        if (live) {
-          tc_fence_after();
-          uint32_t r[32], r2[32];
-          tmem_ld32(tmem + lane_base + (uint32_t)(a * 64), r);
-          tmem_ld32(tmem + lane_base + (uint32_t)(a * 64 + 32), r2);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(b_accempty(a));
+        if (PREP) {
+          // R X (hi / lo) for the dW MMA, from the token's X tile in the stage
+          const bool rx = ok && mbar_wait(b_infull(s), (k / NS) & 1, abort_flag) &&
+                          mbar_wait(b_xrempty(G), (it & 1) ^ 1, abort_flag);
+          if (ok && !rx) {
+            ok = false;
+            raise_error(abort_flag);
+          }
+          if (rx) {
+            const uint32_t xs = sStages + (uint32_t)s * p.stage_bytes + p.dy_bytes;
+            const float4* t4 = reinterpret_cast<const float4*>(tw);
+            for (int task = gt; task < p.H * 8; task += 128) {
+              const int j = task / p.H, row = task - j * p.H;  // neighbours share j: table broadcast
+              const uint32_t off = (uint32_t)row * 128u + (uint32_t)((j ^ (row & 7)) << 4);
+              const uint32_t offl = (uint32_t)(row + 32) * 128u + (uint32_t)((j ^ (row & 7)) << 4);
+              const uint4 xa = *reinterpret_cast<const uint4*>(gen(xs + off));
+              const uint4 xb = *reinterpret_cast<const uint4*>(gen(xs + 4096u + off));
+              const uint32_t av[4] = {xa.x, xa.y, xa.z, xa.w}, bv[4] = {xb.x, xb.y, xb.z, xb.w};
+              uint32_t ah[4], al[4], bh[4], bl[4];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) + __uint_as_float(r2[e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+              for (int e = 0; e < 4; ++e) {
+                // features 8j + 2e, +1 (x0) and their partners 64 + 8j + 2e, +1 (x1)
+                const float4 cs = t4[4 * j + e];
+                const float2 c2 = make_float2(cs.x, cs.y), s2 = make_float2(cs.z, cs.w);
+                const float2 x0 = make_float2(bf16lo_to_f32(av[e]), bf16hi_to_f32(av[e]));
+                const float2 x1 = make_float2(bf16lo_to_f32(bv[e]), bf16hi_to_f32(bv[e]));
+                const float2 ra = __ffma2_rn(x0, c2, __fmul2_rn(make_float2(-x1.x, -x1.y), s2));
+                const float2 rb = __ffma2_rn(x0, s2, __fmul2_rn(x1, c2));
+                ah[e] = pack_bf16x2(ra.x, ra.y);
+                bh[e] = pack_bf16x2(rb.x, rb.y);
+                al[e] = pack_bf16x2(ra.x - bf16lo_to_f32(ah[e]), ra.y - bf16hi_to_f32(ah[e]));
+                bl[e] = pack_bf16x2(rb.x - bf16lo_to_f32(bh[e]), rb.y - bf16hi_to_f32(bh[e]));
+              }
+              // box c of the slot: 64 rows (hi rows 0..31, lo rows 32..63) x 128 B
+              *reinterpret_cast<uint4*>(gen(xr + off)) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+              *reinterpret_cast<uint4*>(gen(xr + 8192u + off)) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
+              *reinterpret_cast<uint4*>(gen(xr + offl)) = make_uint4(al[0], al[1], al[2], al[3]);
+              *reinterpret_cast<uint4*>(gen(xr + 8192u + offl)) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(b_xrfull(G));
+          mbar_arrive(b_inempty(s));
         }
-        if (EXCH) {
-          // inverse rotation: swap with the warp holding features f ^ 64
-          float* mine = reinterpret_cast<float*>(gen(sEx + (uint32_t)(warp * 2 + (it & 1)) * p.ex_bytes));
-          const float* theirs = reinterpret_cast<const float*>(
-              gen(sEx + (uint32_t)((warp ^ 2) * 2 + (it & 1)) * p.ex_bytes));
+        if (DO_DX) {
+          const int a = k % kBwdNA;
+          float c = 1.f, sn = 0.f;
+          if (ROPE) {
+            const int u = f & 63;
+            c = tw[4 * (u >> 1) + (u & 1)];
+            sn = tw[4 * (u >> 1) + 2 + (u & 1)];
+          }
+          const bool live = ok && mbar_wait_warp(b_accfull(a), (k / kBwdNA) & 1, abort_flag);
+          if (ok && !live) {
+            ok = false;
+            raise_error(abort_flag);
+          }
+          float v[32];
+          if (live) {
+            tc_fence_after();
+            uint32_t r[32], r2[32];
+            tmem_ld32(tmem + lane_base + (uint32_t)(a * 64), r);
+            tmem_ld32(tmem + lane_base + (uint32_t)(a * 64 + 32), r2);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(b_accempty(a));
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (e < p.H) mine[e * 32 + lane] = v[e];
-          named_bar_sync(2 + G * 2 + (q & 1), 64);
-          const float sg = f < 64 ? sn : -sn;
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) + __uint_as_float(r2[e]);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (e < p.H) v[e] = fmaf(v[e], c, theirs[e * 32 + lane] * sg);
-        }
-        if (!live) continue;
-        if (lane == 0) bulk_wait_read<1>();  // buffer it & 1 is free again
-        __syncwarp();
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(gen(wout + (uint32_t)(it & 1) * p.out_bytes));
+            for (int e = 0; e < 32; ++e) v[e] = 0.f;
+          }
+          if (EXCH) {
+            // inverse rotation: swap with the warp holding features f ^ 64
+            float* mine = reinterpret_cast<float*>(gen(sEx + (uint32_t)(warp * 2 + (it & 1)) * p.ex_bytes));
+            const float* theirs = reinterpret_cast<const float*>(
+                gen(sEx + (uint32_t)((warp ^ 2) * 2 + (it & 1)) * p.ex_bytes));
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (e < p.H) out[e * 32 + lane] = __float2bfloat16_rn(v[e]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&tmDX, wout + (uint32_t)(it & 1) * p.out_bytes, q * 32, 0, tok);
-          bulk_commit();
+            for (int e = 0; e < 32; ++e)
+              if (e < p.H) mine[e * 32 + lane] = v[e];
+            named_bar_sync(2 + G * 2 + (q & 1), 64);
+            const float sg = f < 64 ? sn : -sn;
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (e < p.H) v[e] = fmaf(v[e], c, theirs[e * 32 + lane] * sg);
+          }
+          if (live) {
+            if (lane == 0) bulk_wait_read<1>();  // buffer it & 1 is free again
+            __syncwarp();
+            __nv_bfloat16* out =
+                reinterpret_cast<__nv_bfloat16*>(gen(wout + (uint32_t)(it & 1) * p.out_bytes));
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (e < p.H) out[e * 32 + lane] = __float2bfloat16_rn(v[e]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmDX, wout + (uint32_t)(it & 1) * p.out_bytes, q * 32, 0, tok);
+              bulk_commit();
+            }
+          }
         }
         // a dW chunk is complete once the last even token of it has passed
-        if (DO_DW && G == 0 && (k + 2 >= n_my || (k + 2) / kDwChunk != k / kDwChunk)) {
+        if (DO_DW && G == 0 && ok && (k + 2 >= n_my || (k + 2) / kDwChunk != k / kDwChunk)) {
           fold_dw(dwc_done);
           ++dwc_done;
           if (!ok) raise_error(abort_flag);
         }
       }
-      if (lane == 0) bulk_wait<0>();
+      if (DO_DX && lane == 0) bulk_wait<0>();
     }
     if (DO_DW && G == 0) {
       for (; ok && dwc_done < n_dwc; ++dwc_done) fold_dw(dwc_done);
@@ -902,6 +929,7 @@ __device__ __forceinline__ void premix_bwd_pass(const CUtensorMap& tmDY, const C
       mbar_inval(b_dwempty(s));
     }
     mbar_inval(b_drain);
+    mbar_inval(b_wt);
   }
   __syncthreads();
 }
@@ -979,7 +1007,7 @@ bool bwd_geometry(int H, int P, bool do_dx, bool do_dw, bool rope, BwdParams* p,
   p->ex_bytes = ((uint32_t)H * 128u + 127u) / 128u * 128u;
   const size_t fixed = 1024 + (do_dx ? (size_t)p->nkb * 8192u : 0) + (prep ? 32768 : 0) +
                        (do_dx ? 16u * p->out_bytes : 0) + (exch ? 16u * p->ex_bytes : 0) +
-                       (prep ? 1024 : 0) + 512;  // last: barriers (<= 2*4 + 25 slots)
+                       (rope ? 2048 : 0) + 512;  // last: barriers (<= 2*4 + 26 slots)
   const size_t limit = kBwdSmemMax;
   p->ns = 4;
   while (p->ns > 2 && fixed + (size_t)p->ns * p->stage_bytes > limit) --p->ns;
