@@ -276,3 +276,32 @@ def joint_attention(yq: np.ndarray, yk: np.ndarray, yv: np.ndarray, causal: bool
     o, lse = attention(view(yq), view(yk), view(yv), MASK_CAUSAL if causal else MASK_NONE, 0,
                        scale)
     return o.reshape(B, N, P, H, d), lse.reshape(B, H, N * P)
+
+
+# ---------------------------------------------------------------- Hiera q_pool
+def q_pool(q: np.ndarray, q_stride: int) -> np.ndarray:
+    """Max-pooled queries of each mask unit ("hiera-optim 0.1.0",
+    hiera_optim/attention/mask_unit.py, MaskUnitAttentionFast.forward with
+    q_stride > 1): a unit's T query rows form q_stride blocks of
+    Tq = T / q_stride rows, the block index being the slow axis, and pooled
+    row t is the elementwise maximum over the blocks of row t of each block
+    (rows t, Tq + t, ..., (q_stride - 1) * Tq + t).
+
+    q [Bo, Bi, T, Hh, d] (float32 or bf16 bits) -> float32 [Bo, Bi, Tq, Hh, d];
+    a maximum picks one of its inputs, so bf16 values stay exact.
+    """
+    qf = _as_f32(q)
+    Bo, Bi, T, Hh, d = qf.shape
+    assert q_stride >= 1 and T % q_stride == 0
+    Tq = T // q_stride
+    return np.ascontiguousarray(qf.reshape(Bo, Bi, q_stride, Tq, Hh, d).max(axis=2))
+
+
+def attention_qpool(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_stride: int,
+                    scale: float | None = None):
+    """Unmasked attention of the pooled queries over all T keys of the unit:
+    ``attention(q_pool(q, q_stride), k, v)`` (the same page and function).
+
+    Returns O [Bo,Bi,Tq,Hh,d] float64 and lse [Bo,Bi,Hh,Tq] float64.
+    """
+    return attention(q_pool(q, q_stride), k, v, MASK_NONE, 0, scale)

@@ -535,3 +535,55 @@ def test_joint_attention_brute_force():
     w = np.exp(s - s.max())
     ref = sum(w[m2] * v[b, m2 // P, m2 % P, h].astype(np.float64) for m2 in range(M)) / w.sum()
     np.testing.assert_allclose(o2[b, n, p, h], ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- Hiera q_pool
+def test_q_pool_stride_one_is_identity_and_blocks_are_the_slow_axis():
+    """q_stride = 1 changes nothing.  With q_stride copies of one block stacked
+    along the slow axis, the pool is that block, while a block made of
+    rows repeated along the fast axis (t * q_stride + i) is not pooled back
+    to itself (the stride is the outer axis of the unit's rows)."""
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((2, 3, 12, 2, 5)).astype(np.float32)
+    np.testing.assert_array_equal(O.q_pool(q, 1), q)
+    blk = rng.standard_normal((2, 3, 4, 2, 5)).astype(np.float32)
+    stacked = np.concatenate([blk, blk, blk], axis=2)          # rows i*4 + t
+    np.testing.assert_array_equal(O.q_pool(stacked, 3), blk)
+    fast = np.repeat(blk, 3, axis=2)                            # rows t*3 + i
+    assert not np.array_equal(O.q_pool(fast, 3), blk)
+
+
+def test_q_pool_takes_the_largest_block_value():
+    """Block i filled with the value i (and a per-row offset): every pooled
+    row is the last block's; the pool never leaves the inputs' values."""
+    S_, Tq = 4, 5
+    q = np.zeros((1, 2, S_ * Tq, 3, 8), np.float32)
+    for i in range(S_):
+        for t in range(Tq):
+            q[:, :, i * Tq + t] = 10.0 * i + t
+    pooled = O.q_pool(q, S_)
+    for t in range(Tq):
+        np.testing.assert_array_equal(pooled[:, :, t], 10.0 * (S_ - 1) + t)
+    # bf16 bit patterns: the result is one of the inputs, exactly
+    bits = (np.random.default_rng(1).integers(0, 0x7F00, (1, 1, 8, 1, 6))).astype(np.uint16)  # finite
+    p = O.q_pool(bits, 2)
+    widened = O._as_f32(bits)
+    assert np.all((p == widened[:, :, :4]) | (p == widened[:, :, 4:]))
+
+
+def test_attention_qpool_with_identical_blocks_is_plain_attention():
+    """Queries made of q_stride identical blocks pool to the block, so the
+    pooled attention equals plain attention of that block over all T keys;
+    q_stride = 1 is plain attention."""
+    rng = np.random.default_rng(5)
+    Bo, Bi, Tq, Hh, d, S_ = 2, 3, 4, 2, 8, 4
+    blk = rng.standard_normal((Bo, Bi, Tq, Hh, d)).astype(np.float32)
+    k = rng.standard_normal((Bo, Bi, Tq * S_, Hh, d)).astype(np.float32)
+    v = rng.standard_normal((Bo, Bi, Tq * S_, Hh, d)).astype(np.float32)
+    q = np.concatenate([blk] * S_, axis=2)
+    o, lse = O.attention_qpool(q, k, v, S_)
+    ro, rl = O.attention(blk, k, v)
+    np.testing.assert_allclose(o, ro, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(lse, rl, rtol=1e-13, atol=1e-13)
+    o1, _ = O.attention_qpool(q, k, v, 1)
+    np.testing.assert_allclose(o1, O.attention(q, k, v)[0], rtol=1e-13, atol=1e-13)
