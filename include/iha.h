@@ -200,6 +200,30 @@ iha_status mha_fwd(const void* q, const void* k, const void* v, void* o,
                    iha_mask mask_mode, int window, iha_dtype dt, void* stream);
 
 /*
+ * Mask-unit attention with pooled queries (Hiera's q_pool; "hiera-optim
+ * 0.1.0", hiera_optim/attention/mask_unit.py, MaskUnitAttentionFast.forward
+ * with q_stride > 1): per (b_outer, b_inner, head) unit of T tokens, the
+ * query rows are max-pooled over q_stride blocks of Tq = T / q_stride rows
+ * (the block index is the slow axis),
+ *   qp[t] = max_i q[i * Tq + t]          (elementwise, i < q_stride)
+ * and attend, unmasked, over all T keys:
+ *   o[t] = sum_j softmax_j(scale * <qp_t, k_j>) v_j,  lse[t] as mha_fwd.
+ * The pooling happens inside the kernel, on the Q tile as it arrives; the
+ * pooled queries are never written to memory.
+ *   q, k, v   bf16 [B_outer, B_inner, T, Hh, d] views (strides sq, sk, sv)
+ *   o         bf16 [B_outer, B_inner, Tq, Hh, d] view (strides so)
+ *   lse_out   nullable; float32 [B_outer, B_inner, Hh, Tq] dense
+ *   scale     <= 0 selects 1/sqrt(d)
+ * Needs T <= 64, q_stride dividing T, d <= 128 and d % 8 == 0; alignment as
+ * mha_fwd.  q_stride = 1 is mha_fwd's unmasked short-sequence attention.
+ */
+iha_status mha_fwd_qpool(const void* q, const void* k, const void* v, void* o,
+                         float* lse_out, int B_outer, int B_inner, int Hh, int T,
+                         int d, int q_stride, iha_strides sq, iha_strides sk,
+                         iha_strides sv, iha_strides so, float scale,
+                         iha_dtype dt, void* stream);
+
+/*
  * Attention backward over Hh heads ("Repository Structure": preprocess,
  * backward, postprocess; "End-to-End Training Benchmark": the training step):
  * with P = softmax(scale Q K^T | mask) recomputed from lse and dO the

@@ -34,7 +34,7 @@ SYMBOLS = ("iha_premix_fwd", "iha_premix_bwd_dx", "iha_premix_bwd_dw", "iha_prem
            "mha_fwd", "mu_gather", "mu_scatter", "iha_status_string", "iha_last_error",
            "iha_device_error", "iha_test_fail_next_wait", "mha_bwd", "mha_bwd_workspace_bytes",
            "mha_bwd_noalloc", "iha_premix_fwd_qkv", "mu_attention_fused",
-           "iha_premix_fwd_qkv_interleaved", "iha_premix_bwd_qkv")
+           "iha_premix_fwd_qkv_interleaved", "iha_premix_bwd_qkv", "mha_fwd_qpool")
 
 
 class IHAError(RuntimeError):
@@ -84,10 +84,12 @@ def lib() -> C.CDLL:
     L.mu_scatter.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, vp]
     L.mu_attention_fused.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
     L.iha_premix_bwd_qkv.argtypes = [vp] * 15 + [i, i, i, i, i, i, i, f, vp]
+    L.mha_fwd_qpool.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, Strides, Strides, Strides,
+                                Strides, f, i, vp]
     for name in ("iha_premix_fwd", "iha_premix_fwd_qkv", "iha_premix_fwd_qkv_interleaved",
                  "iha_premix_bwd_dx",
                  "iha_premix_bwd_dw", "iha_premix_bwd", "mha_fwd", "mha_bwd", "mu_gather",
-                 "mu_scatter", "mu_attention_fused", "iha_premix_bwd_qkv"):
+                 "mu_scatter", "mu_attention_fused", "iha_premix_bwd_qkv", "mha_fwd_qpool"):
         getattr(L, name).restype = C.c_int
     L.iha_status_string.argtypes = [i]
     L.iha_status_string.restype = C.c_char_p
@@ -383,6 +385,39 @@ def mha_fwd(q, k, v, mask: int = MASK_NONE, window: int = 0, scale: float = 0.0,
                         Nk, d, _strides(q5), _strides(k5), _strides(v5), _strides(o5),
                         float(scale), int(mask), int(window), _dt(q), _stream(stream)),
           "mha_fwd")
+    return (out, lse) if return_lse else out
+
+
+def mha_fwd_qpool(q, k, v, q_stride: int, scale: float = 0.0, out=None, lse=None,
+                  return_lse: bool = False, stream=None):
+    """Mask-unit attention with Hiera's pooled queries: q, k, v are [Bo,Bi,T,Hh,d]
+    (or [B,T,Hh,d]) bf16 views; the T query rows are max-pooled over q_stride
+    blocks (block index slow) inside the kernel.  Returns O [Bo,Bi,T/q_stride,Hh,d]
+    (4-D in, 4-D out); with return_lse, also lse [Bo, Bi, Hh, T/q_stride]."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _expect(t, name, q.shape, q.dtype, q.device, contiguous=False)
+    q5, k5, v5 = _as5(q), _as5(k), _as5(v)
+    Bo, Bi, T, Hh, d = q5.shape
+    if q_stride <= 0 or T % q_stride:
+        raise ValueError(f"q_stride {q_stride} must divide T = {T}")
+    Tq = T // q_stride
+    oshape = tuple(q.shape[:-3]) + (Tq, Hh, d)
+    if out is None:
+        out = torch.empty(oshape, dtype=q.dtype, device=q.device)
+    _expect(out, "out", oshape, q.dtype, q.device, contiguous=False)
+    o5 = _as5(out)
+    if lse is None and return_lse:
+        lse = torch.empty((Bo, Bi, Hh, Tq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        if lse.numel() != Bo * Bi * Hh * Tq:
+            raise ValueError(f"lse: {lse.numel()} elements, expected {(Bo, Bi, Hh, Tq)}")
+        _expect(lse, "lse", dtype=torch.float32, device=q.device)
+    check(lib().mha_fwd_qpool(_ptr(q5), _ptr(k5), _ptr(v5), _ptr(o5),
+                              C.c_void_p(lse.data_ptr() if lse is not None else 0), Bo, Bi, Hh,
+                              T, d, int(q_stride), _strides(q5), _strides(k5), _strides(v5),
+                              _strides(o5), float(scale), _dt(q), _stream(stream)),
+          "mha_fwd_qpool")
     return (out, lse) if return_lse else out
 
 

@@ -909,3 +909,31 @@ extern "C" iha_status mha_fwd(const void* q, const void* k, const void* v, void*
   attn_fwd_f32_kernel<<<grid, 128, 0, s>>>(p);
   return check_launch("mha_fwd");
 }
+
+extern "C" iha_status mha_fwd_qpool(const void* q, const void* k, const void* v, void* o,
+                                    float* lse_out, int B_outer, int B_inner, int Hh, int T,
+                                    int d, int q_stride, iha_strides sq, iha_strides sk,
+                                    iha_strides sv, iha_strides so, float scale, iha_dtype dt,
+                                    void* stream) {
+  using namespace iha;
+  if (!q || !k || !v || !o) return fail(IHA_ERR_INVALID_ARG, "mha_fwd_qpool: null pointer");
+  if (B_outer <= 0 || B_inner <= 0 || Hh <= 0 || T <= 0 || d <= 0 || q_stride <= 0)
+    return fail(IHA_ERR_INVALID_ARG, "mha_fwd_qpool: sizes must be positive");
+  if (T % q_stride)
+    return fail(IHA_ERR_INVALID_ARG, "mha_fwd_qpool: q_stride %d does not divide T %d", q_stride,
+                T);
+  if (dt != IHA_BF16) return fail(IHA_ERR_UNSUPPORTED, "mha_fwd_qpool: bf16 only");
+  if (!mu_attention_supported(T, T, d, IHA_MASK_NONE) || d % 8)
+    return fail(IHA_ERR_UNSUPPORTED, "mha_fwd_qpool: needs T <= 64, d <= 128, d %% 8 == 0");
+  if ((int64_t)B_outer * B_inner * Hh > INT32_MAX / 2)
+    return fail(IHA_ERR_UNSUPPORTED, "mha_fwd_qpool: too many units for one launch");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(IHA_ERR_ALIGNMENT, "mha_fwd_qpool: base pointers must be 16-byte aligned");
+  if (!stride_ok(sq, 2) || !stride_ok(sk, 2) || !stride_ok(sv, 2) || !stride_ok(so, 2))
+    return fail(IHA_ERR_ALIGNMENT, "mha_fwd_qpool: strides must be multiples of 8 elements");
+  if (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3))
+    return fail(IHA_ERR_ALIGNMENT, "mha_fwd_qpool: lse_out must be 4-byte aligned");
+  if (!(scale > 0.f)) scale = 1.f / sqrtf((float)d);
+  return mu_attention_fwd(q, k, v, o, lse_out, B_outer, B_inner, Hh, T, d, sq, sk, sv, so, scale,
+                          reinterpret_cast<cudaStream_t>(stream), q_stride);
+}

@@ -20,6 +20,16 @@
 //   warps 4-7  softmax + epilogue of odd pairs (TMEM buffer 1)
 //   warp  8    TMA producer,  warp 9  MMA issuer and TMEM owner
 //
+// Pooled queries (q_stride > 1; "hiera-optim 0.1.0", mask_unit.py,
+// MaskUnitAttentionFast.forward, the q_pool of a pooling block): a unit's T
+// query rows are q_stride blocks of Tq = T / q_stride rows (the block index
+// the slow axis), and the attention uses their elementwise maximum, Tq
+// queries over all T keys.  The pooling runs in the Q tile as it arrives:
+// the softmax warps of the pair's buffer take, for each pooled row t, the
+// maximum of rows t, Tq + t, ... and write it over row t (rows above Tq are
+// only read), then release the tile to the QK^T MMA; rows t >= Tq of S are
+// never stored.
+//
 // Fused mode (FUSED = true): the Hiera stage-1 step gather -> attention ->
 // scatter ("hiera-optim 0.1.0", README, item 2 of what optimize(model) does,
 // and MaskUnitAttentionFast.forward) as one pass.  A kept unit is read
@@ -51,6 +61,7 @@ constexpr int kSmemBytes = 2 * kStageBytes + 256 + 1024;
 
 struct MuParams {
   int Bo, Bi, Hh, T, d, nch, ksteps, npv;
+  int q_stride, Tq;  // pooled queries: Tq = T / q_stride rows stored per unit
   int n_units, n_items;
   float scale_log2;
   int64_t so_bo, so_bi, so_seq, so_h;
@@ -125,7 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto b_ofull = [&](int b) { return bar0 + 8u * (3 * NS + 4 + b); };
   auto b_oempty = [&](int b) { return bar0 + 8u * (3 * NS + 6 + b); };
   const uint32_t b_drain = bar0 + 8u * (3 * NS + 8);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * NS + 10);
+  auto b_qpool = [&](int s) { return bar0 + 8u * (3 * NS + 10 + s); };  // Q of stage s pooled
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * NS + 10 + (FUSED ? 0 : NS));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -144,9 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_oempty(s), 128);
     }
     mbar_init(b_drain, 1);
+    if (!FUSED)
+      for (int s = 0; s < NS; ++s) mbar_init(b_qpool(s), 128);
     *abort_flag = 0;
     mbar_init_fence();
   }
+  const bool pool = !FUSED && p.q_stride > 1;
   if (FUSED && p.T < kRows) {
     // a unit box fills rows 0 .. T-1 of its half; rows T .. 63 are V rows of
     // keys whose P is 0, so they must hold finite values: zero them once
@@ -237,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto ready_qk = [&](int k) {
         const int b = k & 1;
         if (!(ok = mbar_wait_warp(b_qkfull(k % NS), (k / NS) & 1, abort_flag))) return false;
+        if (pool && !(ok = mbar_wait_warp(b_qpool(k % NS), (k / NS) & 1, abort_flag))) return false;
         // S / O of buffer b are free once the epilogue of pair k - 2 has read O
         if (k >= 2 && !(ok = mbar_wait_warp(b_oempty(b), ((k >> 1) - 1) & 1, abort_flag))) return false;
         tc_fence_after();
@@ -281,6 +297,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n = 0;  // pairs of this buffer so far
     for (int k = b; k < n_my; k += 2, ++n) {
       const int item = blockIdx.x + k * gridDim.x;
+      if (pool) {
+        // q_pool of both units' Q in the stage, 16 bytes (8 features) per step
+        const int s = k % NS;
+        if (!(ok = mbar_wait_warp(b_qkfull(s), (k / NS) & 1, abort_flag))) break;
+        uint8_t* st = smem + (uint32_t)s * kSStride;
+        const int n_work = 2 * p.Tq * p.nch * 8;
+        for (int w = row; w < n_work; w += 128) {
+          const int g = w & 7, c = (w >> 3) % p.nch, rest = (w >> 3) / p.nch;
+          const int t = rest % p.Tq, uu = rest / p.Tq;
+          uint8_t* base = st + c * kChunkBytes + uu * kHalfBytes + ((g ^ (t & 7)) << 4);
+          uint4 acc = *reinterpret_cast<const uint4*>(base + t * 128);
+          for (int i = 1; i < p.q_stride; ++i) {
+            const int rr = i * p.Tq + t;
+            const uint4 x = *reinterpret_cast<const uint4*>(
+                st + c * kChunkBytes + uu * kHalfBytes + rr * 128 + ((g ^ (rr & 7)) << 4));
+            acc.x = bf16x2_max(acc.x, x.x);
+            acc.y = bf16x2_max(acc.y, x.y);
+            acc.z = bf16x2_max(acc.z, x.z);
+            acc.w = bf16x2_max(acc.w, x.w);
+          }
+          *reinterpret_cast<uint4*>(base + t * 128) = acc;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(b_qpool(s));
+      }
       const bool live = ok && mbar_wait_warp(b_sfull(b), n & 1, abort_flag);
       if (!live) {
         ok = false;
@@ -349,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ur.valid = false;
       } else {
         ur = unit_ref(p, 2 * item + u);
-        store = ur.valid && r < p.T;
-        orow = p.o + ur.bo * p.so_bo + ur.bi * p.so_bi + (int64_t)min(r, p.T - 1) * p.so_seq +
+        store = ur.valid && r < p.Tq;
+        orow = p.o + ur.bo * p.so_bo + ur.bi * p.so_bi + (int64_t)min(r, p.Tq - 1) * p.so_seq +
                ur.h * p.so_h;
       }
       for (int c = 0; c < p.npv; c += 32) {
@@ -375,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(b_oempty(b));
       if (!FUSED && store && p.lse)
-        p.lse[((int64_t)ur.bz * p.Hh + ur.h) * p.T + r] =
+        p.lse[((int64_t)ur.bz * p.Hh + ur.h) * p.Tq + r] =
             l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
     if (!ok) raise_error(abort_flag);
@@ -417,7 +458,7 @@ bool mu_attention_supported(int Nq, int Nk, int d, int mask) {
 iha_status mu_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                             int Bo, int Bi, int Hh, int T, int d, const iha_strides& sq,
                             const iha_strides& sk, const iha_strides& sv, const iha_strides& so,
-                            float scale, cudaStream_t stream) {
+                            float scale, cudaStream_t stream, int q_stride) {
   CUtensorMap mq, mk, mv;
   if (make_unit_map(&mq, q, Bo, Bi, T, Hh, d, sq) != CUDA_SUCCESS ||
       make_unit_map(&mk, k, Bo, Bi, T, Hh, d, sk) != CUDA_SUCCESS ||
@@ -429,6 +470,8 @@ iha_status mu_attention_fwd(const void* q, const void* k, const void* v, void* o
   p.Hh = Hh;
   p.T = T;
   p.d = d;
+  p.q_stride = q_stride;
+  p.Tq = T / q_stride;
   p.nch = (d + 63) / 64;
   p.ksteps = (d + 15) / 16;
   p.npv = p.ksteps * 16;
@@ -475,6 +518,8 @@ iha_status mu_attention_fused(const void* x, const int32_t* keep, void* canvas, 
   p.Bi = 1;
   p.Hh = 1;
   p.T = mu_h * mu_w;
+  p.q_stride = 1;
+  p.Tq = p.T;
   p.d = C;
   p.nch = (C + 63) / 64;
   p.ksteps = (C + 15) / 16;
