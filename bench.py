@@ -294,7 +294,42 @@ def extra_ops(T, torch, dev, step, device, iters: int, hbm: float, tc: float):
         "frac": round(ideal / (ms * 1e-3), 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
         "bound": "hbm", "l2": "256 MB written between launches",
         "replaces": "mu_gather + mu_attention + mu_scatter (one pass, no gathered copy in HBM)"}}
-    del canvas, flush
+    # Hiera stage-2 pooling block: mask-unit attention with the queries
+    # max-pooled 4:1 inside the kernel, on qkv read in place in Hiera's
+    # [B, T, units, 3, heads, head_dim] layout and O written in its
+    # [B, Tq, units, heads, head_dim] layout
+    hq = S.HIERA_QPOOL
+    gen = torch.Generator(device=device)
+    gen.manual_seed(7)
+    qkv = torch.randn((hq.B, hq.T, hq.n_units, 3, hq.heads, hq.head_dim), generator=gen,
+                      device=device).to(torch.bfloat16)
+    qv, kv, vv = (qkv[:, :, :, c].permute(0, 2, 1, 3, 4) for c in range(3))
+    dst = torch.empty((hq.B, hq.Tq, hq.n_units, hq.heads, hq.head_dim), dtype=torch.bfloat16,
+                      device=device)
+    runq = lambda: T.mha_fwd_qpool(qv, kv, vv, hq.q_stride, out=dst.permute(0, 2, 1, 3, 4))
+    for _ in range(3):
+        runq()
+    ts = []
+    for _ in range(max(iters, 3)):
+        flush.fill_(0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        runq()
+        e1.record()
+        torch.cuda.synchronize(device)
+        ts.append(e0.elapsed_time(e1))
+    ms = statistics.median(ts)
+    units = hq.B * hq.n_units * hq.heads
+    qbytes = units * (3 * hq.T + hq.Tq) * hq.head_dim * 2
+    qflops = 4 * hq.head_dim * hq.Tq * hq.T * units
+    ideal = max(qbytes / hbm, qflops / tc)
+    out["mu_attention_qpool"] = {
+        "config": f"Hiera stage-2 pooling block: B={hq.B}, {hq.n_units} units, T={hq.T} -> "
+                  f"Tq={hq.Tq} (q_stride {hq.q_stride}), {hq.heads} heads of {hq.head_dim}",
+        "ms": round(ms, 5), "roofline_ms": round(ideal * 1e3, 5),
+        "frac": round(ideal / (ms * 1e-3), 4), "GB/s": round(qbytes / (ms * 1e-3) / 1e9, 1),
+        "bound": "hbm", "l2": "256 MB written between launches"}
+    del canvas, flush, qkv, dst
     # joint-softmax variant of the layer forward at the LLaMA shape: premix Q,
     # K (RoPE), V into the interleaved layout, then causal attention of the 20
     # heads over the N*P = 32768 pseudo-tokens

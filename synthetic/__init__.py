@@ -112,6 +112,25 @@ class MaskUnitShape:
 HIERA_MU = MaskUnitShape()
 
 
+@dataclass(frozen=True)
+class QPoolShape:
+    B: int = 128
+    n_units: int = 20       # kept mask units per sample (the MAE keeps 20 of 49)
+    T: int = 64             # tokens per unit entering the block (stage-1 resolution)
+    q_stride: int = 4       # 2 x 2 spatial pooling, flattened
+    heads: int = 2
+    head_dim: int = 96      # dim_out 192 of Hiera-Base stage 2
+
+    @property
+    def Tq(self) -> int:
+        return self.T // self.q_stride
+
+
+# Hiera-Base MAE, first block of stage 2: mask-unit attention whose queries
+# are max-pooled 4:1 (q_stride = 4) over the 64 tokens of each kept unit.
+HIERA_QPOOL = QPoolShape()
+
+
 def premix_weight(H: int, P: int, seed: int, stream: int) -> np.ndarray:
     """W[H, P, H] float32 ~ N(0, 1/H)."""
     return normal((H, P, H), seed, stream, std=1.0 / math.sqrt(H), dtype="f32")
