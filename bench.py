@@ -54,10 +54,10 @@ UNIT = "% of 1-GPU roofline, summed over GPUs"
 # Fraction of every op the oracle runs per CPU sample (same in both CPU legs).
 CPU_FRAC = 1 / 256
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from the one-pass
-# ncu capture in profiles/attn_fwd_tc_causal_B2_N16384_80h_dram.md (removed
-# whenever that kernel changes, until it is captured again).
-NCU_TRAFFIC = {"long_attention_causal": 10517708800 + 673674496}
+# DRAM bytes (read + write) per launch of the dominant kernel, from a one-pass
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the full-size
+# launch; removed whenever that kernel changes, until it is captured again.
+NCU_TRAFFIC = {"long_attention_causal": 2665801984 + 671312640}
 
 
 def load_peaks():
@@ -168,6 +168,7 @@ OP_INPUTS = {
     "mu_attention_fused": ["mu_x", "mu_keep"],
     "long_premix_fwd_qkv": [f"l{a}_{t}" for t in "qkv" for a in "xw"],
     "long_attention_causal": [f"l{a}_{t}" for t in "qkv" for a in "xw"],
+    "mu_attention_qpool": [],   # generated on the device (see qpool_case)
 }
 
 
@@ -263,6 +264,27 @@ class Step:
         done()
 
 
+def qpool_case(T, torch, device):
+    """The Hiera stage-2 pooling block: (enqueue function, algorithmic bytes,
+    flops).  qkv (seeded, on the device) is read in place in Hiera's
+    [B, T, units, 3, heads, head_dim] layout and O written in its
+    [B, Tq, units, heads, head_dim] layout; the queries are max-pooled 4:1
+    inside the kernel."""
+    hq = S.HIERA_QPOOL
+    gen = torch.Generator(device=device)
+    gen.manual_seed(7)
+    qkv = torch.randn((hq.B, hq.T, hq.n_units, 3, hq.heads, hq.head_dim), generator=gen,
+                      device=device).to(torch.bfloat16)
+    qv, kv, vv = (qkv[:, :, :, c].permute(0, 2, 1, 3, 4) for c in range(3))
+    dst = torch.empty((hq.B, hq.Tq, hq.n_units, hq.heads, hq.head_dim), dtype=torch.bfloat16,
+                      device=device)
+    run = lambda: T.mha_fwd_qpool(qv, kv, vv, hq.q_stride, out=dst.permute(0, 2, 1, 3, 4))
+    units = hq.B * hq.n_units * hq.heads
+    nbytes = units * (3 * hq.T + hq.Tq) * hq.head_dim * 2
+    flops = 4 * hq.head_dim * hq.Tq * hq.T * units
+    return run, nbytes, flops
+
+
 def extra_ops(T, torch, dev, step, device, iters: int, hbm: float, tc: float):
     """Ops beyond the step's rows, timed alone after it (not part of `value`):
     the fused gather -> mask-unit attention -> scatter of the Hiera stage-1
@@ -299,14 +321,7 @@ def extra_ops(T, torch, dev, step, device, iters: int, hbm: float, tc: float):
     # [B, T, units, 3, heads, head_dim] layout and O written in its
     # [B, Tq, units, heads, head_dim] layout
     hq = S.HIERA_QPOOL
-    gen = torch.Generator(device=device)
-    gen.manual_seed(7)
-    qkv = torch.randn((hq.B, hq.T, hq.n_units, 3, hq.heads, hq.head_dim), generator=gen,
-                      device=device).to(torch.bfloat16)
-    qv, kv, vv = (qkv[:, :, :, c].permute(0, 2, 1, 3, 4) for c in range(3))
-    dst = torch.empty((hq.B, hq.Tq, hq.n_units, hq.heads, hq.head_dim), dtype=torch.bfloat16,
-                      device=device)
-    runq = lambda: T.mha_fwd_qpool(qv, kv, vv, hq.q_stride, out=dst.permute(0, 2, 1, 3, 4))
+    runq, qbytes, qflops = qpool_case(T, torch, device)
     for _ in range(3):
         runq()
     ts = []
@@ -319,9 +334,6 @@ def extra_ops(T, torch, dev, step, device, iters: int, hbm: float, tc: float):
         torch.cuda.synchronize(device)
         ts.append(e0.elapsed_time(e1))
     ms = statistics.median(ts)
-    units = hq.B * hq.n_units * hq.heads
-    qbytes = units * (3 * hq.T + hq.Tq) * hq.head_dim * 2
-    qflops = 4 * hq.head_dim * hq.Tq * hq.T * units
     ideal = max(qbytes / hbm, qflops / tc)
     out["mu_attention_qpool"] = {
         "config": f"Hiera stage-2 pooling block: B={hq.B}, {hq.n_units} units, T={hq.T} -> "
@@ -329,7 +341,7 @@ def extra_ops(T, torch, dev, step, device, iters: int, hbm: float, tc: float):
         "ms": round(ms, 5), "roofline_ms": round(ideal * 1e3, 5),
         "frac": round(ideal / (ms * 1e-3), 4), "GB/s": round(qbytes / (ms * 1e-3) / 1e9, 1),
         "bound": "hbm", "l2": "256 MB written between launches"}
-    del canvas, flush, qkv, dst
+    del canvas, flush, runq
     # joint-softmax variant of the layer forward at the LLaMA shape: premix Q,
     # K (RoPE), V into the interleaved layout, then causal attention of the 20
     # heads over the N*P = 32768 pseudo-tokens
@@ -765,6 +777,8 @@ def single_op(T, torch, name, dev, device):
         canvas = torch.zeros_like(i["mu_x"])
         return lambda: T.mu_attention_fused(i["mu_x"], i["mu_keep"], canvas, mu.grid_h, mu.grid_w,
                                             mu.mu_h, mu.mu_w)
+    if kind == "mu_attention_qpool":
+        return qpool_case(T, torch, device)[0]
     if kind.startswith("mu_"):
         g, ou = e((mu.B, mu.n_keep, mu.unit_tokens, mu.C)), e((mu.B, mu.n_keep, mu.unit_tokens, mu.C))
         dec = torch.zeros((mu.B, mu.grid_h * mu.grid_w, mu.C), dtype=torch.bfloat16, device=device)
@@ -819,6 +833,10 @@ def single_op_arm(args):
     table["mu_attention_fused"] = (2 * mu.B * mu.n_keep * mu.unit_tokens * mu.C * 2 +
                                    mu.B * mu.n_keep * 4,
                                    4 * mu.C * mu.unit_tokens ** 2 * mu.B * mu.n_keep)
+    hq = S.HIERA_QPOOL
+    units = hq.B * hq.n_units * hq.heads
+    table["mu_attention_qpool"] = (units * (3 * hq.T + hq.Tq) * hq.head_dim * 2,
+                                   4 * hq.head_dim * hq.Tq * hq.T * units)
     nbytes, flops = table[args.only]
     ms = e0.elapsed_time(e1) / args.steps
     out = {"op": args.only, "ms": round(ms, 5), "GB/s": round(nbytes / ms / 1e6, 1),

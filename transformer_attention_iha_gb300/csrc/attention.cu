@@ -37,7 +37,6 @@
 #include <math.h>
 
 #include <mutex>
-#include <type_traits>
 
 #include "common.cuh"
 #include "mu_attention.h"
@@ -128,24 +127,25 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int idx) {
   return it;
 }
 
-// Visible columns a .. a + 31 of a row whose visible columns are [c_lo, c_hi]
-// (bit e for column a + e).
-__device__ __forceinline__ uint32_t chunk_vis(int a, int c_lo, int c_hi) {
-  const int lo = min(max(c_lo - a, 0), 32), hi = min(max(c_hi - a + 1, 0), 32);
-  return (hi >= 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u)) &
-         ~(lo >= 32 ? 0xFFFFFFFFu : ((1u << lo) - 1u));
-}
-
-// -inf outside the visible columns of a row (bits of `vis`) for the 32
-// scores s[0..31] of one chunk.  A row's visible columns form one interval
-// and a warp holds 32 consecutive rows, so most chunks are visible or hidden
-// for the whole warp: a chunk visible to the whole warp is left alone (a
-// warp-uniform test; callers skip the hidden ones), and only chunks that the
-// interval's edge crosses pay a select per score.
-__device__ __forceinline__ void mask_sel(uint32_t* s, uint32_t vis) {
-  if (__any_sync(0xffffffffu, vis != 0xFFFFFFFFu)) {
+// -inf outside the visible columns [c_lo, c_hi] of a row, for NC chunks of 32
+// scores starting at column c0.  A row's visible columns form one interval
+// and a warp holds 32 consecutive rows, so most chunks are visible (or
+// hidden) for the whole warp: those take a warp-uniform shortcut, and only
+// the chunks the interval edge crosses pay a select per score.
+template <int NC>
+__device__ __forceinline__ void mask_cols(uint32_t* s, int c0, int c_lo, int c_hi) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) s[e] = (vis >> e) & 1u ? s[e] : 0xFF800000u;
+  for (int cc = 0; cc < NC; ++cc) {
+    const int a = c0 + 32 * cc;
+    // visible columns of this chunk, bits lo .. hi - 1
+    const int lo = min(max(c_lo - a, 0), 32), hi = min(max(c_hi - a + 1, 0), 32);
+    const uint32_t vis = (hi >= 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u)) &
+                         ~(lo >= 32 ? 0xFFFFFFFFu : ((1u << lo) - 1u));
+    if (__any_sync(0xffffffffu, vis != 0xFFFFFFFFu)) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        s[32 * cc + e] = (vis >> e) & 1u ? s[32 * cc + e] : 0xFF800000u;
+    }
   }
 }
 
@@ -501,120 +501,81 @@ __global__ void __launch_bounds__(kThreads, 1)
              (k0 + kBN - 1 <= tq_lo && (p.mask == IHA_MASK_CAUSAL || tq_hi - k0 < p.window)));
         // visible columns of this tile for this row: [c_lo, c_hi]
         const int c_lo = max(key_lo - k0, 0), c_hi = min(key_hi - k0, kBN - 1);
-        // One softmax step over S: full tiles take the plain path; tiles that
-        // the mask cuts take a copy that skips the 32-column chunks hidden
-        // from the whole warp (no exponentials, P = 0) and selects per score
-        // only in the chunks the visible interval's edge crosses.
-        auto step = [&](auto masked_tag) {
-          constexpr bool kMasked = decltype(masked_tag)::value;
-          // pass 1: row maximum
-          float mt;
-          {
-            uint32_t s[128];
+        // pass 1: row maximum (the whole row, four independent max chains)
+        float mt;
+        {
+          uint32_t s[128];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s + 32 * c);
-            tmem_wait_ld();
-            if constexpr (kMasked) {
-              float mx[2] = {-INFINITY, -INFINITY};
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s + 32 * c);
+          tmem_wait_ld();
+          if (!full_tile) mask_cols<4>(s, 0, c_lo, c_hi);
+          float mx[4];
 #pragma unroll
-              for (int cc = 0; cc < 4; ++cc) {
-                const uint32_t vis = chunk_vis(32 * cc, c_lo, c_hi);
-                if (__all_sync(0xffffffffu, vis == 0u)) continue;
-                mask_sel(s + 32 * cc, vis);
+          for (int q = 0; q < 4; ++q) mx[q] = __uint_as_float(s[q]);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
+          for (int e = 4; e < 128; e += 8)
 #pragma unroll
-                  for (int q = 0; q < 2; ++q)
-                    mx[q] = fmax3f(mx[q], __uint_as_float(s[32 * cc + e + q]),
-                                   __uint_as_float(s[32 * cc + e + 2 + q]));
-              }
-              mt = fmaxf(mx[0], mx[1]);
+            for (int q = 0; q < 4; ++q)
+              mx[q] = fmax3f(mx[q], __uint_as_float(s[e + q]), __uint_as_float(s[e + 4 + q]));
+          mt = fmaxf(fmax3f(mx[0], mx[1], mx[2]), mx[3]);
+        }
+        const float m_new = fmaxf(m_used, mt * sl2);
+        bool rescale = false;
+        float factor = 1.f;
+        if (j == lo_t) {
+          m_used = m_new;
+        } else if (__any_sync(0xffffffffu, m_new > m_used + kRescaleLog2)) {
+          factor = (m_new == -INFINITY) ? 1.f : fast_exp2(m_used - m_new);
+          l *= factor;
+          m_used = m_new;
+          rescale = true;
+        }
+        const float base = (m_used == -INFINITY) ? 0.f : m_used;
+        // pass 2, by halves of 64 columns: P = 2^(s * scale_log2 - base),
+        // packed to bf16 pairs over the S columns (P half h lands in columns
+        // 32h .. 32h+31, below every S column still to be read); pairs 3, 7,
+        // 11, 15 of every 16 use the FMA-pipe polynomial.
+        const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(-base, -base);
+        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t s[64];
+          tmem_ld32(tS + 64u * h, s);
+          tmem_ld32(tS + 64u * h + 32u, s + 32);
+          tmem_wait_ld();
+          if (!full_tile) mask_cols<2>(s, 64 * h, c_lo, c_hi);
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float2 xx = __ffma2_rn(
+                make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nb2);
+            float2 pp;
+            if ((e & 3) == 3) {
+              pp = exp2_poly3_x2(xx);
             } else {
-              // four independent max chains over the whole row
-              float mx[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) mx[q] = __uint_as_float(s[q]);
-#pragma unroll
-              for (int e = 4; e < 128; e += 8)
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  mx[q] = fmax3f(mx[q], __uint_as_float(s[e + q]), __uint_as_float(s[e + 4 + q]));
-              mt = fmaxf(fmax3f(mx[0], mx[1], mx[2]), mx[3]);
+              pp.x = fast_exp2(xx.x);
+              pp.y = fast_exp2(xx.y);
             }
+            sum2[e & 1] = __fadd2_rn(sum2[e & 1], pp);
+            pk[e] = pack_bf16x2(pp.x, pp.y);
           }
-          const float m_new = fmaxf(m_used, mt * sl2);
-          bool rescale = false;
-          float factor = 1.f;
-          if (j == lo_t) {
-            m_used = m_new;
-          } else if (__any_sync(0xffffffffu, m_new > m_used + kRescaleLog2)) {
-            factor = (m_new == -INFINITY) ? 1.f : fast_exp2(m_used - m_new);
-            l *= factor;
-            m_used = m_new;
-            rescale = true;
-          }
-          const float base = (m_used == -INFINITY) ? 0.f : m_used;
-          // pass 2, by halves of 64 columns: P = 2^(s * scale_log2 - base),
-          // packed to bf16 pairs over the S columns (P half h lands in columns
-          // 32h .. 32h+31, below every S column still to be read); pairs 3, 7,
-          // 11, 15 of every 16 use the FMA-pipe polynomial.
-          const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(-base, -base);
-          float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          tmem_st32(tS + 32u * h, pk);
+        }
+        const float2 st = __fadd2_rn(sum2[0], sum2[1]);
+        l += st.x + st.y;
+        if (rescale) {
+          // O <- O * factor before this tile's P.V is issued (P.V of the
+          // previous tile is complete: the S commit waited on above tracks it)
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t s[64];
-            tmem_ld32(tS + 64u * h, s);
-            tmem_ld32(tS + 64u * h + 32u, s + 32);
+          for (int c = 0; c < 2 * NCH; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + 32u * c, r);
             tmem_wait_ld();
-            uint32_t pk[32];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              if constexpr (kMasked) {
-                const uint32_t vis = chunk_vis(64 * h + 32 * cc, c_lo, c_hi);
-                if (__all_sync(0xffffffffu, vis == 0u)) {
-#pragma unroll
-                  for (int e = 16 * cc; e < 16 * cc + 16; ++e) pk[e] = 0u;
-                  continue;
-                }
-                mask_sel(s + 32 * cc, vis);
-              }
-#pragma unroll
-              for (int e = 16 * cc; e < 16 * cc + 16; ++e) {
-                const float2 xx = __ffma2_rn(
-                    make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc2, nb2);
-                float2 pp;
-                if ((e & 3) == 3) {
-                  pp = exp2_poly3_x2(xx);
-                } else {
-                  pp.x = fast_exp2(xx.x);
-                  pp.y = fast_exp2(xx.y);
-                }
-                sum2[e & 1] = __fadd2_rn(sum2[e & 1], pp);
-                pk[e] = pack_bf16x2(pp.x, pp.y);
-              }
-            }
-            tmem_st32(tS + 32u * h, pk);
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
+            tmem_st32(tO + 32u * c, r);
           }
-          const float2 st = __fadd2_rn(sum2[0], sum2[1]);
-          l += st.x + st.y;
-          if (rescale) {
-            // O <- O * factor before this tile's P.V is issued (P.V of the
-            // previous tile is complete: the S commit waited on above tracks it)
-#pragma unroll
-            for (int c = 0; c < 2 * NCH; ++c) {
-              uint32_t r[32];
-              tmem_ld32(tO + 32u * c, r);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
-              tmem_st32(tO + 32u * c, r);
-            }
-          }
-        };
-        if (full_tile)
-          step(std::false_type{});
-        else
-          step(std::true_type{});
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(b_pfull(t));
