@@ -855,7 +855,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--cpu-frac", type=float, default=CPU_FRAC,
                     help="fraction of every op each oracle sample runs")
     ap.add_argument("--cpu-samples", type=int, default=2,
