@@ -265,3 +265,21 @@ def test_attention_work_counter_slots_are_reused(T):
                 assert torch.equal(t, first), f"launch {n}"
     torch.cuda.synchronize()
     assert T.device_error() == 0
+
+
+@pytest.mark.parametrize("shape", [(1, 384, 3, 128), (2, 1030, 5, 64), (1, 4096, 4, 128)])
+def test_attention_window_one_returns_v_exactly(T, shape):
+    """W = 1: each query sees only its own key, the softmax has one term
+    (P = 1), so O is V bit for bit and lse is the scaled self-score.  Holds at
+    any size; catches a row maximum taken over masked scores (P rounded
+    away from 1) that the bf16 tolerance would let through."""
+    import torch
+    B, N, Hh, d = shape
+    q, k, v = _qkv((B, N, Hh, d), (B, N, Hh, d), seed=N + Hh)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    o, lse = T.mha_fwd(qd, kd, vd, mask=O.MASK_CAUSAL_WINDOW, window=1, return_lse=True)
+    assert torch.equal(o, vd)
+    s = (qd.float() * kd.float()).sum(-1) / np.sqrt(d)          # [B, N, Hh]
+    np.testing.assert_allclose(lse[:, 0].cpu().numpy(), s.permute(0, 2, 1).cpu().numpy(),
+                               atol=2e-4, rtol=1e-5)
+    assert T.device_error() == 0

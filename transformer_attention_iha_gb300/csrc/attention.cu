@@ -127,40 +127,26 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int idx) {
   return it;
 }
 
-// Visible columns a .. a + 31 of a row whose visible columns are [c_lo, c_hi]
-// (bit e for column a + e).
-__device__ __forceinline__ uint32_t chunk_vis(int a, int c_lo, int c_hi) {
-  const int lo = min(max(c_lo - a, 0), 32), hi = min(max(c_hi - a + 1, 0), 32);
-  return (hi >= 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u)) &
-         ~(lo >= 32 ? 0xFFFFFFFFu : ((1u << lo) - 1u));
-}
-
-// Applies the mask to a 128-column S tile in tensor memory (this warp's 32
-// lanes at tS): -inf outside each row's visible columns [c_lo, c_hi].  A row's
-// visible columns form one interval and a warp holds 32 consecutive rows, so
-// most 32-column chunks are visible (left alone) or hidden (overwritten with
-// -inf) for the whole warp; only chunks that the interval's edge crosses are
-// read back and selected per score.  The softmax then runs the same code as
-// for an unmasked tile (exp of -inf is 0), so the rarely taken masked case
-// adds only this short, compact loop.
-__device__ __forceinline__ void mask_tile_tmem(uint32_t tS, int c_lo, int c_hi) {
-#pragma unroll 1
-  for (int cc = 0; cc < 4; ++cc) {
-    const uint32_t vis = chunk_vis(32 * cc, c_lo, c_hi);
-    if (__all_sync(0xffffffffu, vis == 0xFFFFFFFFu)) continue;
-    uint32_t r[32];
-    if (__all_sync(0xffffffffu, vis == 0u)) {
+// -inf outside the visible columns [c_lo, c_hi] of a row, for NC chunks of 32
+// scores starting at column c0.  A row's visible columns form one interval
+// and a warp holds 32 consecutive rows, so most chunks are visible (or
+// hidden) for the whole warp: those take a warp-uniform shortcut, and only
+// the chunks the interval edge crosses pay a select per score.
+template <int NC>
+__device__ __forceinline__ void mask_cols(uint32_t* s, int c0, int c_lo, int c_hi) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) r[e] = 0xFF800000u;
-    } else {
-      tmem_ld32(tS + 32u * cc, r);
-      tmem_wait_ld();
+  for (int cc = 0; cc < NC; ++cc) {
+    const int a = c0 + 32 * cc;
+    // visible columns of this chunk, bits lo .. hi - 1
+    const int lo = min(max(c_lo - a, 0), 32), hi = min(max(c_hi - a + 1, 0), 32);
+    const uint32_t vis = (hi >= 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u)) &
+                         ~(lo >= 32 ? 0xFFFFFFFFu : ((1u << lo) - 1u));
+    if (__any_sync(0xffffffffu, vis != 0xFFFFFFFFu)) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) r[e] = (vis >> e) & 1u ? r[e] : 0xFF800000u;
+      for (int e = 0; e < 32; ++e)
+        s[32 * cc + e] = (vis >> e) & 1u ? s[32 * cc + e] : 0xFF800000u;
     }
-    tmem_st32(tS + 32u * cc, r);
   }
-  tmem_wait_st();
 }
 
 __device__ __forceinline__ void raise_error(volatile int* abort_flag) {
@@ -513,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             (k0 + kBN <= p.Nk) &&
             (p.mask == IHA_MASK_NONE ||
              (k0 + kBN - 1 <= tq_lo && (p.mask == IHA_MASK_CAUSAL || tq_hi - k0 < p.window)));
-        if (!full_tile)  // visible columns of this row: [c_lo, c_hi]
-          mask_tile_tmem(tS, max(key_lo - k0, 0), min(key_hi - k0, kBN - 1));
+        // visible columns of this tile for this row: [c_lo, c_hi]
+        const int c_lo = max(key_lo - k0, 0), c_hi = min(key_hi - k0, kBN - 1);
         // pass 1: row maximum (the whole row, four independent max chains)
         float mt;
         {
@@ -522,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s + 32 * c);
           tmem_wait_ld();
+          if (!full_tile) mask_cols<4>(s, 0, c_lo, c_hi);
           float mx[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) mx[q] = __uint_as_float(s[q]);
@@ -556,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tS + 64u * h, s);
           tmem_ld32(tS + 64u * h + 32u, s + 32);
           tmem_wait_ld();
+          if (!full_tile) mask_cols<2>(s, 64 * h, c_lo, c_hi);
           uint32_t pk[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
