@@ -270,15 +270,17 @@ def test_attention_work_counter_slots_are_reused(T):
 @pytest.mark.parametrize("shape", [(1, 384, 3, 128), (2, 1030, 5, 64), (1, 4096, 4, 128)])
 def test_attention_window_one_returns_v_exactly(T, shape):
     """W = 1: each query sees only its own key, the softmax has one term
-    (P = 1), so O is V bit for bit and lse is the scaled self-score.  Holds at
-    any size; catches a row maximum taken over masked scores (P rounded
-    away from 1) that the bf16 tolerance would let through."""
+    (P = 1), so O is V and lse the scaled self-score.  Holds at any size;
+    catches a row maximum taken over masked scores (P rounded away from 1,
+    O off by a bf16 ulp ~1e-2) that the bf16 tolerance would let through.
+    The one allowed difference is the weight a masked key keeps in the
+    FMA-pipe exponential, 2^-125 (about 1e-38) instead of 0."""
     import torch
     B, N, Hh, d = shape
     q, k, v = _qkv((B, N, Hh, d), (B, N, Hh, d), seed=N + Hh)
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
     o, lse = T.mha_fwd(qd, kd, vd, mask=O.MASK_CAUSAL_WINDOW, window=1, return_lse=True)
-    assert torch.equal(o, vd)
+    assert float((o.float() - vd.float()).abs().max()) <= 1e-30
     s = (qd.float() * kd.float()).sum(-1) / np.sqrt(d)          # [B, N, Hh]
     np.testing.assert_allclose(lse[:, 0].cpu().numpy(), s.permute(0, 2, 1).cpu().numpy(),
                                atol=2e-4, rtol=1e-5)
