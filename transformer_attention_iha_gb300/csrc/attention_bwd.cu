@@ -29,8 +29,11 @@
 //              share the lanes and take query columns 0-63 / 64-127), dK / dV
 //              epilogue (feature columns split the same way)
 //   warps 8-11 dQ^T drain (thread = feature = TMEM lane): staged in the tile's
-//              Q / dO stage, added into dQ_acc by one TMA reduce-add a tile
-//   warp  12   TMA producer (K, V once per item; Q, dO per query tile, 2 stages)
+//              Q / dO stage (queries 0-63 in the Q half, 64-127 in the dO
+//              half), added into dQ_acc by two TMA reduce-adds a tile; each
+//              half goes back to the producer once its reduction has read it
+//   warp  12   TMA producer (K, V once per item; Q, dO per query tile, 2 stages,
+//              Q and dO each with their own full / empty barriers)
 //   warp  13   tcgen05.mma issuer and TMEM owner
 // TMEM (512 columns): regions R0 | R1 rotate S^T / dP^T / dQ^T between query
 // tiles; dK at 256, dV at 384.  One shared 128 x 128 bf16 tile holds P^T,
@@ -152,7 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // starts; the MMA, compute and drain warps take them in order
   auto b_ifull = [&](int s) { return bar0 + 8u * (20 + s); };
   auto b_iempty = [&](int s) { return bar0 + 8u * (24 + s); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 28);
+  // dO has its own full / empty pair: the two halves of a stage are handed
+  // back separately (Q once the first half of dQ^T has been reduced from it,
+  // dO once the second half has)
+  auto b_dofull = [&](int s) { return bar0 + 8u * (28 + s); };
+  auto b_doempty = [&](int s) { return bar0 + 8u * (30 + s); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* item_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);
   unsigned int* work = g_work[p.work_slot];
@@ -165,7 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_kvempty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(b_qfull(s), 1);
-      mbar_init(b_qempty(s), 1);  // the dQ reduction has read the stage
+      mbar_init(b_qempty(s), 1);  // the first dQ reduction has read the Q half
+      mbar_init(b_dofull(s), 1);
+      mbar_init(b_doempty(s), 1);  // the second one has read the dO half
       mbar_init(b_dqfull(s), 1);
       mbar_init(b_dqempty(s), 128);
     }
@@ -236,16 +246,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int qt = it.qlo; qt <= it.qhi; ++qt, ++nq) {
           const int s = nq & 1;
           if (nq >= 2 && !(ok = mbar_wait(b_qempty(s), ((nq >> 1) - 1) & 1, abort_flag))) break;
-          mbar_arrive_expect_tx(b_qfull(s), 2 * tile_bytes + 2 * kB * 4);
+          mbar_arrive_expect_tx(b_qfull(s), tile_bytes + 2 * kB * 4);
           const int64_t row0 = (int64_t)it.hb * p.Npad + qt * kB;  // 512-byte aligned
           bulk_load(sLD + (uint32_t)s * 2 * kB * 4, p.lse2 + row0, kB * 4, b_qfull(s));
           bulk_load(sLD + (uint32_t)s * 2 * kB * 4 + kB * 4, p.Dv + row0, kB * 4, b_qfull(s));
-          for (int c = 0; c < p.nch; ++c) {
+          for (int c = 0; c < p.nch; ++c)
             tma_load_4d(sQ + 2 * s * kTileB + c * kChunkB, &tmQ, b_qfull(s), c * 64, qt * kB, it.h,
                         it.b);
-            tma_load_4d(sDO + 2 * s * kTileB + c * kChunkB, &tmDO, b_qfull(s), c * 64, qt * kB, it.h,
-                        it.b);
-          }
+          if (nq >= 2 && !(ok = mbar_wait(b_doempty(s), ((nq >> 1) - 1) & 1, abort_flag))) break;
+          mbar_arrive_expect_tx(b_dofull(s), tile_bytes);
+          for (int c = 0; c < p.nch; ++c)
+            tma_load_4d(sDO + 2 * s * kTileB + c * kChunkB, &tmDO, b_dofull(s), c * 64, qt * kB,
+                        it.h, it.b);
         }
         if (!ok) break;
         idx = nxt;
@@ -254,8 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // no copy may still be landing when the CTA exits
       volatile int no_abort = 0;
       if (ni > 0) mbar_wait(b_kvfull, (ni - 1) & 1, &no_abort);
-      for (uint32_t n = nq > 2 ? nq - 2 : 0; n < nq; ++n)
+      for (uint32_t n = nq > 2 ? nq - 2 : 0; n < nq; ++n) {
         mbar_wait(b_qfull(n & 1), (n >> 1) & 1, &no_abort);
+        mbar_wait(b_dofull(n & 1), (n >> 1) & 1, &no_abort);
+      }
     }
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
@@ -292,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dP^T = V dO^T into the region dQ^T of the previous tile used
           if (gt >= 1 && !(ok = mbar_wait_warp(b_dqempty(r ^ 1), ((gt - 1) >> 1) & 1, abort_flag)))
             break;
+          if (!(ok = mbar_wait_warp(b_dofull(s), (gt >> 1) & 1, abort_flag))) break;
           tc_fence_after();
           {
             const uint64_t da = smem_desc_sw128(sV, 16, 1024), db = smem_desc_sw128(do_s, 16, 1024);
@@ -493,12 +508,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 12) {
     // ------------------------------------------------------------ dQ^T drain (warps 8-11)
     // Once dQ^T(t) is complete, every MMA that reads tile t's Q / dO stage
-    // has finished, so the stage (64 KB, contiguous) becomes the staging
-    // area: rows = queries, d fp32 features each, thread = feature writes its
-    // column.  When all 128 drain threads have written (b_stg), one thread
-    // adds the whole tile into dQ_acc with a single TMA reduce-add (box
-    // d x 128; the reduction runs in the bulk-copy engine, not as 16 K element
-    // atomics) and hands the stage back to the producer once it has been read.
+    // has finished, so the stage becomes the staging area: queries 0-63 in
+    // the Q half, 64-127 in the dO half, rows = queries of d fp32 features,
+    // thread = feature writes its column.  When all 128 drain threads have
+    // written (b_stg), one thread adds the tile into dQ_acc with two TMA
+    // reduce-adds (boxes d x 64; the reduction runs in the bulk-copy engine,
+    // not as element atomics) and hands each half back to the producer as
+    // soon as its reduction has read it: the next Q tile can land while the
+    // second half is still being reduced.
     const int wq = warp - 8;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const int feat = wq * 32 + lane;
@@ -511,7 +528,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int qt = it.qlo; qt <= it.qhi; ++qt, ++gt) {
         const int r = gt & 1, s = gt & 1;
         const uint32_t stage_s = sQ + 2u * (uint32_t)s * kTileB;
-        float* stage = reinterpret_cast<float*>(smem + (stage_s - sK));
         if (!(ok = mbar_wait_warp(b_dqfull(r), (gt >> 1) & 1, abort_flag))) break;
         tc_fence_after();
 #pragma unroll 1
@@ -520,8 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + lane_base + 128u * r + 32u * c, v);
           tmem_wait_ld();
           if (feat < p.d) {
+            float* half = reinterpret_cast<float*>(smem + (stage_s - sK) + (c >> 1) * kTileB);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) stage[(32 * c + e) * p.d + feat] = __uint_as_float(v[e]);
+            for (int e = 0; e < 32; ++e)
+              half[(32 * (c & 1) + e) * p.d + feat] = __uint_as_float(v[e]);
           }
         }
         tc_fence_before();
@@ -532,8 +550,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((ok = mbar_wait(b_stg, gt & 1, abort_flag))) {
             tma_reduce_add_4d(&tmDQ, stage_s, 0, qt * kB, it.h, it.b);
             bulk_commit();
-            bulk_wait_read<0>();     // the reduce has read the staging
-            mbar_arrive(b_qempty(s));  // the stage is the producer's again
+            const bool second = qt * kB + 64 < p.N;  // rows past N: nothing to add
+            if (second) {
+              tma_reduce_add_4d(&tmDQ, stage_s + kTileB, 0, qt * kB + 64, it.h, it.b);
+              bulk_commit();
+              bulk_wait_read<1>();  // the first reduce has read the Q half
+            } else {
+              bulk_wait_read<0>();
+            }
+            mbar_arrive(b_qempty(s));   // the Q half is the producer's again
+            bulk_wait_read<0>();        // the second has read the dO half
+            mbar_arrive(b_doempty(s));
           }
         }
         if (wq == 0) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;  // warp-uniform
@@ -661,10 +688,10 @@ iha_status mha_bwd_launch(const void* q, const void* k, const void* v, const voi
   }
   CUtensorMap mq, mk, mv, mdo, mdq;
   {
-    // dQ_acc [B, N, Hh, d] fp32, box d features x 128 queries, no swizzle
+    // dQ_acc [B, N, Hh, d] fp32, box d features x 64 queries, no swizzle
     uint64_t dims[4] = {(uint64_t)d, (uint64_t)N, (uint64_t)Hh, (uint64_t)B};
     uint64_t st[3] = {(uint64_t)Hh * d * 4, (uint64_t)d * 4, (uint64_t)N * Hh * d * 4};
-    uint32_t box[4] = {(uint32_t)d, 128, 1, 1};
+    uint32_t box[4] = {(uint32_t)d, 64, 1, 1};
     if (encode_tiled(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, st, box,
                      CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
       return fail(IHA_ERR_CUDA, "mha_bwd: dQ accumulator tensor map encoding failed");
