@@ -102,3 +102,38 @@ def test_attention_bwd_rejects_bad_args(T):
     assert L.mha_bwd(p(q), p(q), p(q), p(q), p(q), p(lse), p(q), p(outs[1]), p(outs[2]), p(ws),
                      need, 1, 2, 8, 64, 0.0, 1, 0, 1, None) == 1
     assert T.device_error() == 0
+
+
+def test_attention_bwd_work_counter_slots_are_reused(T):
+    """The backward's items (one key tile of one head) past the first wave
+    come from a per-launch counter that the last CTA resets: 300 launches on
+    two streams (every slot of the 256-entry counter table taken more than
+    once) must reproduce the first launch's dK and dV bit for bit (each key
+    tile's dK / dV is summed by one CTA in a fixed order) and its dQ to
+    rounding (dQ is added by reductions in whatever order CTAs finish)."""
+    import torch
+    B, N, Hh, d, mask, window = 2, 1030, 48, 128, O.MASK_CAUSAL_WINDOW, 300
+    q, k, v, g = (S.normal((B, N, Hh, d), 31, c) for c in range(4))
+    qd, kd, vd, gd = (to_dev(a) for a in (q, k, v, g))
+    o, lse = T.mha_fwd(qd, kd, vd, mask=mask, window=window, return_lse=True)
+    dq0, dk0, dv0 = T.mha_bwd(qd, kd, vd, o, gd, lse, mask=mask, window=window)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    outs = [tuple(torch.empty_like(dq0) for _ in range(3)) for _ in range(2)]
+    wss = [torch.empty(T.mha_bwd_workspace_bytes(B, Hh, N, d), dtype=torch.uint8, device="cuda")
+           for _ in range(2)]
+    for n in range(300):
+        with torch.cuda.stream(streams[n & 1]):
+            dq, dk, dv = outs[n & 1]
+            T.mha_bwd(qd, kd, vd, o, gd, lse, mask=mask, window=window, dq=dq, dk=dk, dv=dv,
+                      workspace=wss[n & 1])
+        if n % 60 == 59 or n >= 298:
+            torch.cuda.synchronize()
+            for dq, dk, dv in outs:
+                assert torch.equal(dk, dk0) and torch.equal(dv, dv0), f"launch {n}"
+                # one bf16 ulp at most (2^-7 relative): the fp32 sums differ in order only
+                diff = (dq.float() - dq0.float()).abs()
+                assert bool((diff <= 2.0 ** -7 * dq0.float().abs() + 1e-6).all()), f"launch {n}"
+    torch.cuda.synchronize()
+    assert T.device_error() == 0
