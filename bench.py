@@ -432,32 +432,49 @@ class ClockSampler:
 
 
 def tiny_layer_latency(T, torch, device, iters: int = 50):
-    """Tiny fp32 IHA layer forward (premix Q, K, V into 8 pseudo-heads, then
-    unmasked attention): microseconds per layer (4 launches), CUDA events."""
+    """Tiny fp32 IHA layer forward (premix Q, K, V into 8 pseudo-heads in one
+    launch, then unmasked attention): microseconds per layer, CUDA events.
+    Its two kernels take a few microseconds each, so issued one call at a time the
+    layer waits on the host; the layer is captured once in a CUDA graph and
+    replayed (`us_per_layer`), and the eager time is reported beside it."""
     sh = S.TINY
     xs = [host_tensor(S.normal((sh.B, sh.N, sh.H, sh.d), 0, c, dtype="f32"), torch).to(device)
           for c in range(3)]
     ws = [host_tensor(S.premix_weight(sh.H, sh.P, 0, 10 + c), torch).to(device) for c in range(3)]
-    ys = [torch.empty((sh.B, sh.N, sh.HP, sh.d), dtype=torch.float32, device=device)
-          for _ in range(3)]
+    ys = tuple(torch.empty((sh.B, sh.N, sh.HP, sh.d), dtype=torch.float32, device=device)
+               for _ in range(3))
     o = torch.empty_like(ys[0])
 
     def layer():
-        for x, w, y in zip(xs, ws, ys):
-            T.premix_fwd(x, w, sh.P, out=y)
+        T.premix_fwd_qkv(xs, ws, sh.P, out=ys)
         T.mha_fwd(*ys, out=o)
 
-    for _ in range(5):
+    def timed(run):
+        stream = torch.cuda.current_stream(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        for _ in range(iters):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) * 1e3 / iters
+
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        for _ in range(5):
+            layer()
+    torch.cuda.current_stream(device).wait_stream(side)
+    eager = timed(layer)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
         layer()
+    graph.replay()
     torch.cuda.synchronize(device)
-    stream = torch.cuda.current_stream(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(iters):
-        layer()
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    return {"us_per_layer": round(e0.elapsed_time(e1) * 1e3 / iters, 2), "launches": 4,
+    replay = timed(graph.replay)
+    return {"us_per_layer": round(replay, 2), "us_per_layer_eager": round(eager, 2),
+            "launches": 2, "how": "CUDA graph of the layer replayed (eager: one call at a time)",
             "config": "B=1, N=128, H=4, P=2, d=32, fp32, unmasked"}
 
 

@@ -95,7 +95,8 @@ iha_status iha_premix_fwd(const void* x, const float* w, void* y, int B, int N,
  * for (x_t, w_t, y_t); RoPE (when rope != 0) is applied to q and k only.
  * All nine buffers follow iha_premix_fwd's layout and limits; no output may
  * overlap any input or another output.  Shapes outside the tensor-core
- * kernel run as three launches of the CUDA-core kernel on the same stream.
+ * kernel run on the CUDA-core kernel: Q, K and V in one launch (with RoPE,
+ * Q and K in one and V in a second), on the same stream.
  */
 iha_status iha_premix_fwd_qkv(const void* xq, const void* xk, const void* xv,
                               const float* wq, const float* wk, const float* wv,

@@ -651,18 +651,23 @@ struct AttnF32Params {
 
 constexpr int kF32Rows = 32, kF32Keys = 32;
 
+// DQ: a bound on the features per thread (d / 4), so that the per-thread
+// query and accumulator arrays are indexed by unrolled loops and stay in
+// registers (a runtime-bounded loop over them puts them in local memory).
+template <int DQ>
 __global__ void __launch_bounds__(128) attn_fwd_f32_kernel(const AttnF32Params p) {
   __shared__ float ks[kF32Keys][128 + 1];
   __shared__ float vs[kF32Keys][128 + 1];
   const int quad = threadIdx.x >> 2, qi = threadIdx.x & 3;
-  const int dq = p.d >> 2;  // features per thread
+  const int dq = p.d >> 2;  // features per thread (<= DQ)
   const int h = blockIdx.y;
   const int bz = blockIdx.z, bo = bz / p.Bi, bi = bz - bo * p.Bi;
   const int i = blockIdx.x * kF32Rows + quad;
   const bool valid = i < p.Nq;
-  float qv[32], acc[32];
+  float qv[DQ], acc[DQ];
   const float* qrow = p.q + bo * p.sq.b_outer + bi * p.sq.b_inner + (int64_t)min(i, p.Nq - 1) * p.sq.seq + h * p.sq.head;
-  for (int e = 0; e < 32; ++e) {
+#pragma unroll
+  for (int e = 0; e < DQ; ++e) {
     qv[e] = (e < dq) ? qrow[qi * dq + e] : 0.f;
     acc[e] = 0.f;
   }
@@ -685,10 +690,16 @@ __global__ void __launch_bounds__(128) attn_fwd_f32_kernel(const AttnF32Params p
       vs[kr][f] = vvv;
     }
     __syncthreads();
+    // the chunk's 32 scores first (independent, so their dot products and
+    // shuffles overlap), then one rescale and the chunk's P.V
+    float sc[kF32Keys];
+#pragma unroll
     for (int kr = 0; kr < kF32Keys; ++kr) {
       const int kj = kb + kr;
       float dot = 0.f;
-      for (int e = 0; e < dq; ++e) dot = fmaf(qv[e], ks[kr][qi * dq + e], dot);
+#pragma unroll
+      for (int e = 0; e < DQ; ++e)
+        if (e < dq) dot = fmaf(qv[e], ks[kr][qi * dq + e], dot);
       dot += __shfl_xor_sync(0xffffffffu, dot, 1);
       dot += __shfl_xor_sync(0xffffffffu, dot, 2);
       bool vis = kj < p.Nk;
@@ -696,20 +707,33 @@ __global__ void __launch_bounds__(128) attn_fwd_f32_kernel(const AttnF32Params p
         vis = vis && kj <= i;
         if (p.mask == IHA_MASK_CAUSAL_WINDOW) vis = vis && (i - kj < p.window);
       }
-      if (!vis) continue;
-      const float s = dot * p.scale;
-      const float m_new = fmaxf(m, s);
-      const float corr = expf(m - m_new);
-      const float pe = expf(s - m_new);
-      l = l * corr + pe;
-      for (int e = 0; e < dq; ++e) acc[e] = fmaf(pe, vs[kr][qi * dq + e], acc[e] * corr);
-      m = m_new;
+      sc[kr] = vis ? dot * p.scale : -INFINITY;
     }
+    float mc = sc[0];
+#pragma unroll
+    for (int kr = 1; kr < kF32Keys; ++kr) mc = fmaxf(mc, sc[kr]);
+    if (mc == -INFINITY) continue;  // no visible key in this chunk for this row
+    const float m_new = fmaxf(m, mc);
+    const float corr = expf(m - m_new);
+    l *= corr;
+#pragma unroll
+    for (int e = 0; e < DQ; ++e) acc[e] *= corr;
+#pragma unroll
+    for (int kr = 0; kr < kF32Keys; ++kr) {
+      const float pe = expf(sc[kr] - m_new);  // 0 for a hidden key
+      l += pe;
+#pragma unroll
+      for (int e = 0; e < DQ; ++e)
+        if (e < dq) acc[e] = fmaf(pe, vs[kr][qi * dq + e], acc[e]);
+    }
+    m = m_new;
   }
   if (valid) {
     float* orow = p.o + bo * p.so.b_outer + bi * p.so.b_inner + (int64_t)i * p.so.seq + h * p.so.head;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    for (int e = 0; e < dq; ++e) orow[qi * dq + e] = acc[e] * inv;
+#pragma unroll
+    for (int e = 0; e < DQ; ++e)
+      if (e < dq) orow[qi * dq + e] = acc[e] * inv;
     if (p.lse && qi == 0) p.lse[((int64_t)bz * p.Hh + h) * p.Nq + i] = l > 0.f ? m + logf(l) : -INFINITY;
   }
 }
@@ -867,7 +891,17 @@ extern "C" iha_status mha_fwd(const void* q, const void* k, const void* v, void*
   p.o = static_cast<float*>(o);
   p.lse = lse_out;
   dim3 grid((Nq + kF32Rows - 1) / kF32Rows, Hh, B_outer * B_inner);
-  attn_fwd_f32_kernel<<<grid, 128, 0, s>>>(p);
+  const int dq = d / 4;
+  if (dq <= 2)
+    attn_fwd_f32_kernel<2><<<grid, 128, 0, s>>>(p);
+  else if (dq <= 4)
+    attn_fwd_f32_kernel<4><<<grid, 128, 0, s>>>(p);
+  else if (dq <= 8)
+    attn_fwd_f32_kernel<8><<<grid, 128, 0, s>>>(p);
+  else if (dq <= 16)
+    attn_fwd_f32_kernel<16><<<grid, 128, 0, s>>>(p);
+  else
+    attn_fwd_f32_kernel<32><<<grid, 128, 0, s>>>(p);
   return check_launch("mha_fwd");
 }
 

@@ -90,14 +90,22 @@ __device__ __forceinline__ void stage_w(float* wsm, const float* __restrict__ w,
 // ---------------------------------------------------------------- forward
 // Thread = (token, 4 consecutive features).  Threads of one token are
 // consecutive lanes of one warp when d/4 divides 32 (always for RoPE), so
-// the RoPE partner (feature f +- d/2) is lane ^ (d/8).
+// the RoPE partner (feature f +- d/2) is lane ^ (d/8).  blockIdx.y picks one
+// of up to three tensors (Q, K, V) of the launch, each with its own X, W, Y.
+template <typename T>
+struct FwdTensors {
+  const T* x[3];
+  const float* w[3];
+  T* y[3];
+};
+
 template <typename T, int HC, bool ROPE>
-__global__ void __launch_bounds__(256) premix_fwd_kernel(const T* __restrict__ x,
-                                                         const float* __restrict__ w,
-                                                         T* __restrict__ y, PremixGeom g) {
+__global__ void __launch_bounds__(256) premix_fwd_kernel(const FwdTensors<T> ts, PremixGeom g) {
   extern __shared__ float4 smem_f4[];
   float* wsm = reinterpret_cast<float*>(smem_f4);
-  stage_w<HC>(wsm, w, g);
+  const T* __restrict__ x = ts.x[blockIdx.y];
+  T* __restrict__ y = ts.y[blockIdx.y];
+  stage_w<HC>(wsm, ts.w[blockIdx.y], g);
 
   const int tpt = g.d >> 2;
   const int64_t total = g.ntok * tpt;
@@ -494,20 +502,32 @@ unsigned slot_grid(const PremixGeom& g, int threads) {
   }
 
 template <typename T>
-void launch_fwd(const PremixGeom& g, const void* x, const float* w, void* y, bool rope,
-                cudaStream_t s) {
+void launch_fwd_n(const PremixGeom& g, int ntens, const void* const* x, const float* const* w,
+                  void* const* y, bool rope, cudaStream_t s) {
   const int threads = 256;
   const unsigned blocks = slot_grid(g, threads);
   const int hc = pick_hc(g.H);
   const size_t smem = (size_t)g.HP * hc * sizeof(float);
+  FwdTensors<T> ts;
+  for (int t = 0; t < 3; ++t) {
+    const int u = t < ntens ? t : 0;
+    ts.x[t] = static_cast<const T*>(x[u]);
+    ts.w[t] = w[u];
+    ts.y[t] = static_cast<T*>(y[u]);
+  }
+  const dim3 grid(blocks, ntens);
   IHA_HC_SWITCH(hc, {
     if (rope)
-      premix_fwd_kernel<T, kHC, true><<<blocks, threads, smem, s>>>(
-          static_cast<const T*>(x), w, static_cast<T*>(y), g);
+      premix_fwd_kernel<T, kHC, true><<<grid, threads, smem, s>>>(ts, g);
     else
-      premix_fwd_kernel<T, kHC, false><<<blocks, threads, smem, s>>>(
-          static_cast<const T*>(x), w, static_cast<T*>(y), g);
+      premix_fwd_kernel<T, kHC, false><<<grid, threads, smem, s>>>(ts, g);
   })
+}
+
+template <typename T>
+void launch_fwd(const PremixGeom& g, const void* x, const float* w, void* y, bool rope,
+                cudaStream_t s) {
+  launch_fwd_n<T>(g, 1, &x, &w, &y, rope, s);
 }
 
 template <typename T>
@@ -620,14 +640,16 @@ iha_status iha_premix_fwd_qkv(const void* xq, const void* xk, const void* xv, co
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dt == IHA_BF16 && premix_tc_supported(H, P, d))
     return premix_fwd_tc_multi(3, x, w, y, B, N, H, P, d, rope ? 3 : 0, rope_base, s);
-  for (int t = 0; t < 3; ++t) {
-    const bool r = t < 2 && rope;
-    if (dt == IHA_BF16) launch_fwd<__nv_bfloat16>(g, x[t], w[t], y[t], r, s);
-    else launch_fwd<float>(g, x[t], w[t], y[t], r, s);
-    const iha_status st = check_launch("iha_premix_fwd_qkv");
-    if (st != IHA_OK) return st;
-  }
-  return IHA_OK;
+  // CUDA-core kernel: Q, K and V in one launch, or Q, K (rotated) in one and
+  // V in another when RoPE is on
+  const int n_first = rope ? 2 : 3;
+  if (dt == IHA_BF16) launch_fwd_n<__nv_bfloat16>(g, n_first, x, w, y, rope != 0, s);
+  else launch_fwd_n<float>(g, n_first, x, w, y, rope != 0, s);
+  iha_status st = check_launch("iha_premix_fwd_qkv");
+  if (st != IHA_OK || !rope) return st;
+  if (dt == IHA_BF16) launch_fwd_n<__nv_bfloat16>(g, 1, x + 2, w + 2, y + 2, false, s);
+  else launch_fwd_n<float>(g, 1, x + 2, w + 2, y + 2, false, s);
+  return check_launch("iha_premix_fwd_qkv");
 }
 
 iha_status iha_premix_fwd_qkv_interleaved(const void* xq, const void* xk, const void* xv,
