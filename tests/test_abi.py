@@ -108,3 +108,38 @@ def test_python_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(mod._build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         mod.lib()
+
+
+def test_premix_qkv_backward_validation(L):
+    """iha_premix_bwd_qkv checks all fifteen buffers on the host."""
+    def call(dyk=FAKE, H=4, P=2, d=32, dt=T.BF16, dwv=FAKE, rope=0):
+        return L.iha_premix_bwd_qkv(FAKE, dyk, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                    FAKE, FAKE, FAKE, FAKE, FAKE, dwv, 1, 8, H, P, d, dt, rope,
+                                    1e4, None)
+    assert call(dyk=None) == 1
+    assert call(H=33, P=1) == 2
+    assert call(H=20, P=7) == 2
+    assert call(dt=7) == 1
+    assert call(d=96, rope=1) == 2                # RoPE needs d a power of two
+    assert call(dwv=MISALIGNED) == 3
+    assert call() == 1                            # every buffer at one address
+    assert "overlap" in _err(L)
+
+
+def test_qpool_attention_validation(L):
+    """mha_fwd_qpool rejects what the pooled mask-unit kernel cannot run."""
+    s = _s(64 * 96 * 2, 64 * 96 * 2, 96, 96)
+
+    def call(q=FAKE, T_=64, d=96, qs=4, dt=T.BF16, lse=None, sq=s):
+        return L.mha_fwd_qpool(q, FAKE, FAKE, FAKE, lse, 1, 1, 1, T_, d, qs, sq, s, s, s, 0.0,
+                               dt, None)
+    assert call(q=None) == 1
+    assert call(qs=0) == 1
+    assert call(qs=3) == 1                        # 3 does not divide 64
+    assert "q_stride" in _err(L)
+    assert call(dt=T.F32) == 2
+    assert call(T_=128, qs=4) == 2                # more than 64 tokens per unit
+    assert call(d=12, qs=4) == 2
+    assert call(q=MISALIGNED) == 3
+    assert call(lse=C.c_void_p(0x10002)) == 3
+    assert call(sq=_s(64 * 96 * 2, 64 * 96 * 2, 100, 96)) == 3   # stride not 8-aligned
