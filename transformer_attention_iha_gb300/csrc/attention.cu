@@ -509,14 +509,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32u * c, s + 32 * c);
           tmem_wait_ld();
           if (!full_tile) mask_cols<4>(s, 0, c_lo, c_hi);
+          // chain q takes columns q, q + 4, ...: 0-3 to start, two more
+          // per step over 4-123, and 124-127 last
           float mx[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) mx[q] = __uint_as_float(s[q]);
 #pragma unroll
-          for (int e = 4; e < 128; e += 8)
+          for (int e = 4; e < 124; e += 8)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               mx[q] = fmax3f(mx[q], __uint_as_float(s[e + q]), __uint_as_float(s[e + 4 + q]));
+#pragma unroll
+          for (int q = 0; q < 4; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(s[124 + q]));
           mt = fmaxf(fmax3f(mx[0], mx[1], mx[2]), mx[3]);
         }
         const float m_new = fmaxf(m_used, mt * sl2);

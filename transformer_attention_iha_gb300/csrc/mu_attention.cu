@@ -336,14 +336,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 64; ++e) s[e] = sel_u32(e >= p.T, 0xFF800000u, s[e]);
       }
+      // chain qq takes columns qq, qq + 4, ...: 0-3 to start, two more per
+      // step over 4-59, and 60-63 last
       float mx[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) mx[e] = __uint_as_float(s[e]);
 #pragma unroll
-      for (int e = 4; e < 64; e += 8)
+      for (int e = 4; e < 60; e += 8)
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq)
           mx[qq] = fmax3f(mx[qq], __uint_as_float(s[e + qq]), __uint_as_float(s[e + 4 + qq]));
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) mx[qq] = fmaxf(mx[qq], __uint_as_float(s[60 + qq]));
       const float m = fmaxf(fmax3f(mx[0], mx[1], mx[2]), mx[3]) * sl2;
       const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(-m, -m);
       float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
