@@ -1,4 +1,5 @@
-// Tensor-core premix forward for bf16 tensors with d in {64, 128}.
+// Tensor-core premix for bf16 tensors: the forward (d in {64, 128}) here,
+// the backward (d = 128) in the second half of the file.
 //
 // "IHA-CUDA: Interleaved Head Attention Kernels for Hopper GPUs", section
 // "Pseudo-Token Mixing (Triton Premix Kernels)": Y[b,n,h*P+p,f] =
