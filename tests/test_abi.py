@@ -143,3 +143,71 @@ def test_qpool_attention_validation(L):
     assert call(q=MISALIGNED) == 3
     assert call(lse=C.c_void_p(0x10002)) == 3
     assert call(sq=_s(64 * 96 * 2, 64 * 96 * 2, 100, 96)) == 3   # stride not 8-aligned
+
+
+def _declarations():
+    """{name: (return type, [parameter types])} of every function in include/."""
+    out = {}
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if not f.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for ret, name, params in re.findall(
+                r"^\s*((?:const\s+)?\w+\s*\*?)\s*(\w+)\s*\(([^)]*)\)\s*;", src, flags=re.M):
+            types = []
+            for prm in params.split(","):
+                prm = " ".join(prm.split())
+                if prm in ("", "void"):
+                    continue
+                types.append(re.sub(r"\s*\w+$", "", prm).replace(" *", "*"))
+            out[name] = (" ".join(ret.split()).replace(" *", "*"), types)
+    return out
+
+
+_CTYPE = {"int": C.c_int, "float": C.c_float, "size_t": C.c_size_t,
+          "iha_dtype": C.c_int, "iha_mask": C.c_int, "iha_status": C.c_int,
+          "const char*": C.c_char_p, "iha_strides": T.Strides}
+
+
+def _expected(ctype: str):
+    return C.c_void_p if ctype.endswith("*") and ctype != "const char*" else _CTYPE[ctype]
+
+
+def test_binding_signatures_match_the_header(L):
+    """Every ctypes argtypes / restype the binding sets agrees, parameter by
+    parameter, with the C declaration: a pointer is a c_void_p, an enum or int
+    a c_int, a float a c_float, size_t a c_size_t, iha_strides the struct."""
+    decl = _declarations()
+    assert set(T.SYMBOLS) <= set(decl)
+    checked = 0
+    for name, (ret, params) in decl.items():
+        fn = getattr(L, name)
+        assert fn.argtypes is not None, f"{name}: argtypes not set"
+        assert len(fn.argtypes) == len(params), (name, params, fn.argtypes)
+        for i, (got, ctype) in enumerate(zip(fn.argtypes, params)):
+            assert got is _expected(ctype), f"{name} parameter {i}: {ctype} bound as {got}"
+        assert fn.restype is _expected(ret), f"{name}: returns {ret}, bound as {fn.restype}"
+        checked += 1
+    assert checked == len(decl) >= 19
+
+
+def test_strides_struct_matches_the_header():
+    src = open(os.path.join(ROOT, "include", "iha.h")).read()
+    body = re.search(r"typedef struct \{(.*?)\} iha_strides;", src, flags=re.S).group(1)
+    fields = re.findall(r"int64_t\s+(\w+);", body)
+    assert [(n, t) for n, t in T.Strides._fields_] == [(f, C.c_int64) for f in fields]
+
+
+@pytest.mark.parametrize("compiler,std", [("gcc", "-std=c99"), ("g++", "-std=c++11")])
+def test_header_is_plain_c_and_cpp(compiler, std, tmp_path):
+    import shutil
+    import subprocess
+    if shutil.which(compiler) is None:
+        pytest.skip(f"{compiler} not found")
+    src = tmp_path / ("t.c" if compiler == "gcc" else "t.cpp")
+    src.write_text('#include "iha.h"\nint main(void) { return IHA_OK; }\n')
+    r = subprocess.run([compiler, std, "-Wall", "-Werror", "-pedantic", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
