@@ -865,7 +865,7 @@ def single_op_arm(args):
 
 
 # --------------------------------------------------------------------------- main
-def main():
+def make_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1,
                     help="GPUs of the run; must equal WORLD_SIZE (torchrun) when > 1")
@@ -880,6 +880,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=sorted(OP_INPUTS),
                     help="time one op of the step alone on one GPU (profiling case)")
+    return ap
+
+
+def main():
+    ap = make_parser()
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

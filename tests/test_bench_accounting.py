@@ -15,8 +15,15 @@ activations, fp32 weights, fp32 LSE, int32 keep ids); FLOPs count 2 per
 multiply-add of the contractions the path defines.  The values are written
 out here from those shapes, not taken from the bench's inputs, so a wrong
 shape or a dropped term in the bench's table fails.
+
+The last test keeps the ncu summaries under profiles/ reproducible: every
+command they quote runs committed files, with flags the bench still takes,
+and every ncu command leaves the GPU clocks alone.
 """
+import glob
 import os
+import shlex
+import subprocess
 import sys
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -100,3 +107,53 @@ def test_every_step_op_is_accounted():
         "mu_gather", "mu_attention", "mu_scatter", "long_premix_fwd_qkv",
         "long_attention_causal"])
     assert bench.launches_per_step() == 12
+
+
+def _profile_commands():
+    """Every command quoted in profiles/*.md (indented blocks, continuation
+    lines joined), as (file, command) pairs."""
+    out = []
+    for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        lines = open(f).read().splitlines()
+        block = []
+        for ln in lines + [""]:
+            if ln.startswith("    "):
+                block.append(ln.strip())
+            elif block:
+                text = " ".join(b[:-1].strip() if b.endswith("\\") else b for b in block)
+                out += [(f, c.strip()) for c in text.split("&&") if c.strip()]
+                block = []
+    return out
+
+
+def _committed(path: str) -> bool:
+    r = subprocess.run(["git", "ls-files", "--error-unmatch", path], cwd=ROOT,
+                       capture_output=True, text=True)
+    if r.returncode == 0:
+        return True
+    inside = subprocess.run(["git", "rev-parse", "--is-inside-work-tree"], cwd=ROOT,
+                            capture_output=True, text=True)
+    # outside a git checkout (an exported tree): the file must at least exist
+    return inside.returncode != 0 and os.path.exists(os.path.join(ROOT, path))
+
+
+def test_profile_commands_run_committed_files_with_current_flags():
+    import bench
+    cmds = _profile_commands()
+    files = {os.path.basename(f) for f, _ in cmds}
+    assert files == {os.path.basename(f) for f in glob.glob(os.path.join(ROOT, "profiles", "*.md"))}
+    ap = bench.make_parser()
+    for f, c in cmds:
+        argv = shlex.split(c)
+        assert "_work" not in c, (f, c)
+        if argv[0] == "ncu":
+            assert "--clock-control" in argv and argv[argv.index("--clock-control") + 1] == "none", (f, c)
+        if "bench.py" in argv:
+            rest = argv[argv.index("bench.py") + 1:]
+            try:
+                ap.parse_args(rest)
+            except SystemExit:
+                raise AssertionError(f"{os.path.basename(f)}: bench.py {' '.join(rest)}")
+        for a in argv:
+            if a.endswith(".py") and not a.startswith("-"):
+                assert _committed(a), (f, a)
