@@ -587,3 +587,56 @@ def test_attention_qpool_with_identical_blocks_is_plain_attention():
     np.testing.assert_allclose(lse, rl, rtol=1e-13, atol=1e-13)
     o1, _ = O.attention_qpool(q, k, v, 1)
     np.testing.assert_allclose(o1, O.attention(q, k, v)[0], rtol=1e-13, atol=1e-13)
+
+
+_THREADS_SCRIPT = r"""
+import sys, pickle
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+import oracle as O
+import synthetic as S
+B, N, H, P, d = 2, 37, 5, 3, 16
+x = S.normal((B, N, H, d), 11, 0)
+dy = S.normal((B, N, H * P, d), 11, 1)
+w = S.premix_weight(H, P, 11, 2)
+q, k, v, g = (S.normal((1, 45, 3, 16), 12, c) for c in range(4))
+o, lse = O.attention(q[:, None], k[:, None], v[:, None], O.MASK_CAUSAL_WINDOW, 9)
+grid = S.normal((2, 16, 6), 13, 0)
+keep = S.keep_units(2, 4, 2, 13)
+out = {
+    "threads": O.num_threads(),
+    "fwd": O.premix_fwd(x, w, P, rope=True),
+    "dx": O.premix_bwd_dx(dy, w, rope=True),
+    "dw": O.premix_bwd_dw(dy, x, P, rope=True),
+    "o": o, "lse": lse,
+    "bwd": O.attention_bwd(q, k, v, g, O.MASK_CAUSAL_WINDOW, 9),
+    "gather": O.mu_gather(grid, keep, 4, 4, 2, 2),
+}
+sys.stdout.buffer.write(pickle.dumps(out))
+"""
+
+
+def test_oracle_does_not_depend_on_its_thread_count():
+    """Every oracle output is computed by one thread in a fixed order, except
+    dW, whose per-thread slabs are summed in slab order: so one thread and
+    four give bit-identical results, and dW agrees to double rounding.  A
+    race in any of the parallel loops would break this."""
+    import os
+    import pickle
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = []
+    for n in ("1", "4"):
+        env = dict(os.environ, OMP_NUM_THREADS=n)
+        r = subprocess.run([sys.executable, "-c", _THREADS_SCRIPT, root], env=env,
+                           capture_output=True, timeout=300)
+        assert r.returncode == 0, r.stderr.decode()
+        res.append(pickle.loads(r.stdout))
+    a, b = res
+    assert (a["threads"], b["threads"]) == (1, 4)
+    for key in ("fwd", "dx", "o", "lse", "gather"):
+        assert np.array_equal(a[key], b[key]), key
+    for ga, gb in zip(a["bwd"], b["bwd"]):
+        assert np.array_equal(ga, gb)
+    np.testing.assert_allclose(a["dw"], b["dw"], rtol=1e-13, atol=1e-13 * np.abs(a["dw"]).max())
