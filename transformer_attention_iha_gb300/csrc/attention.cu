@@ -765,20 +765,14 @@ CUresult make_map(CUtensorMap* m, const void* base, int Bo, int Bi, int N, int H
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-std::once_flag g_tc_attr_once;
-cudaError_t g_tc_attr_err = cudaSuccess;
+SmemLimit g_tc_limit[2];
 
-// Dynamic shared memory attribute of both instantiations, set once per
-// process (thread-safe); the size does not depend on the device.
+// Dynamic shared memory limit of both instantiations on the current device
+// (set on the device's first launch, thread-safe).
 cudaError_t set_tc_attributes() {
-  std::call_once(g_tc_attr_once, [] {
-    g_tc_attr_err = cudaFuncSetAttribute(attn_fwd_tc_kernel<1>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (g_tc_attr_err == cudaSuccess)
-      g_tc_attr_err = cudaFuncSetAttribute(attn_fwd_tc_kernel<2>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  });
-  return g_tc_attr_err;
+  cudaError_t e = g_tc_limit[0].ensure(attn_fwd_tc_kernel<1>, kSmemBytes);
+  if (e == cudaSuccess) e = g_tc_limit[1].ensure(attn_fwd_tc_kernel<2>, kSmemBytes);
+  return e;
 }
 
 iha_status launch_tc(const void* q, const void* k, const void* v, void* o, float* lse, int Bo,

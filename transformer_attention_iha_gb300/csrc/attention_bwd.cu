@@ -653,8 +653,7 @@ WsLayout ws_layout(int B, int Hh, int N, int d) {
   return w;
 }
 
-std::once_flag g_attr_once;
-cudaError_t g_attr_err = cudaSuccess;
+SmemLimit g_bwd_limit;  // dynamic shared memory limit of attn_bwd_tc_kernel, per device
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -728,12 +727,9 @@ iha_status mha_bwd_launch(const void* q, const void* k, const void* v, const voi
   p.dq_acc = dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
-  std::call_once(g_attr_once, [] {
-    g_attr_err = cudaFuncSetAttribute(attn_bwd_tc_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  });
-  if (g_attr_err != cudaSuccess)
-    return fail(IHA_ERR_CUDA, "mha_bwd (smem attribute): %s", cudaGetErrorString(g_attr_err));
+  const cudaError_t attr_err = g_bwd_limit.ensure(attn_bwd_tc_kernel, kSmemBytes);
+  if (attr_err != cudaSuccess)
+    return fail(IHA_ERR_CUDA, "mha_bwd (smem attribute): %s", cudaGetErrorString(attr_err));
   int grid = sm_count();
   if (grid > p.n_items) grid = p.n_items;
   attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, p);

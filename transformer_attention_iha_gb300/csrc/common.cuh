@@ -9,6 +9,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "iha.h"
 
@@ -60,6 +61,32 @@ constexpr int kWorkSlots = 256;
     static std::atomic<unsigned int> seq{0};                                    \
     return seq.fetch_add(1u, std::memory_order_relaxed) % ::iha::kWorkSlots;    \
   }
+
+// A kernel's dynamic shared-memory limit, raised on each device the first
+// time the kernel is launched there: the attribute belongs to the kernel's
+// instance in that device's context, so one call per process would leave a
+// second device of the same process at the default limit.  The first caller
+// on a device sets it under the lock; later callers see the device's bit.
+class SmemLimit {
+ public:
+  template <typename F>
+  cudaError_t ensure(F* kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done_.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    std::lock_guard<std::mutex> lk(mu_);
+    if (bit != 0 && (done_.load(std::memory_order_relaxed) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done_.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::atomic<uint64_t> done_{0};  // bit d: set on device d
+  std::mutex mu_;
+};
 
 #define IHA_DEVICE_ERROR_WORD(tag)                                              \
   static __device__ unsigned int g_dev_error;                                   \

@@ -213,13 +213,9 @@ iha_status mu_launch(const void* from, const int32_t* keep, void* to, int B, int
     if (blocks > bg.n_bk) blocks = bg.n_bk;
     const size_t smem = (size_t)kStages * unit_bytes;
     auto kern = mu_bulk_kernel<GATHER>;
-    // the ring's largest size, set once per kernel (thread-safe)
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-      attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      kStages * kStageMax);
-    });
+    // the ring's largest size, set on each device's first launch (thread-safe)
+    static SmemLimit limit;
+    const cudaError_t attr_err = limit.ensure(kern, kStages * kStageMax);
     if (attr_err != cudaSuccess)
       return fail(IHA_ERR_CUDA, "%s (smem attribute): %s", name, cudaGetErrorString(attr_err));
     kern<<<blocks, 32, smem, s>>>(static_cast<const uint8_t*>(from), keep,

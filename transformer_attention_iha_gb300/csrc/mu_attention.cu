@@ -450,8 +450,15 @@ CUresult make_unit_map(CUtensorMap* m, const void* base, int Bo, int Bi, int T, 
                       box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-std::once_flag g_attr_once;
-cudaError_t g_attr_err = cudaSuccess;
+SmemLimit g_mu_limit[2];
+
+// Dynamic shared memory limit of both instantiations on the current device
+// (set on the device's first launch, thread-safe).
+cudaError_t set_mu_attributes() {
+  cudaError_t e = g_mu_limit[0].ensure(mu_attn_kernel<false>, kSmemBytes);
+  if (e == cudaSuccess) e = g_mu_limit[1].ensure(mu_attn_kernel<true>, kSmemBytes);
+  return e;
+}
 
 }  // namespace
 
@@ -489,15 +496,9 @@ iha_status mu_attention_fwd(const void* q, const void* k, const void* v, void* o
   p.so_h = so.head;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
-  std::call_once(g_attr_once, [] {
-    g_attr_err = cudaFuncSetAttribute(mu_attn_kernel<false>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (g_attr_err == cudaSuccess)
-      g_attr_err = cudaFuncSetAttribute(mu_attn_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  });
-  if (g_attr_err != cudaSuccess)
-    return fail(IHA_ERR_CUDA, "mha_fwd (smem attribute): %s", cudaGetErrorString(g_attr_err));
+  const cudaError_t attr_err = set_mu_attributes();
+  if (attr_err != cudaSuccess)
+    return fail(IHA_ERR_CUDA, "mha_fwd (smem attribute): %s", cudaGetErrorString(attr_err));
   int grid = sm_count();
   if (grid > p.n_items) grid = p.n_items;
   mu_attn_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
@@ -543,16 +544,10 @@ iha_status mu_attention_fused(const void* x, const int32_t* keep, void* canvas, 
   p.grid_w = grid_w;
   p.B = B;
   p.G = (int64_t)grid_h * grid_w;
-  std::call_once(g_attr_once, [] {
-    g_attr_err = cudaFuncSetAttribute(mu_attn_kernel<false>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (g_attr_err == cudaSuccess)
-      g_attr_err = cudaFuncSetAttribute(mu_attn_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  });
-  if (g_attr_err != cudaSuccess)
+  const cudaError_t attr_err = set_mu_attributes();
+  if (attr_err != cudaSuccess)
     return fail(IHA_ERR_CUDA, "mu_attention_fused (smem attribute): %s",
-                cudaGetErrorString(g_attr_err));
+                cudaGetErrorString(attr_err));
   int grid = sm_count();
   if (grid > p.n_items) grid = p.n_items;
   mu_attn_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(mx, mx, mx, p);

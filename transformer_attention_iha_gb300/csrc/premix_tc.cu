@@ -423,15 +423,8 @@ iha_status premix_fwd_tc_multi(int ntens, const void* const* x, const float* con
   const size_t smem = fixed + (size_t)p.x_stages * p.stage_bytes;
   if (smem > 227 * 1024) return fail(IHA_ERR_UNSUPPORTED, "premix forward: shared memory budget");
   auto kern = d == 128 ? premix_fwd_tc_kernel<128> : premix_fwd_tc_kernel<64>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {  // both instantiations, once per process
-    attr_err = cudaFuncSetAttribute(premix_fwd_tc_kernel<128>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(premix_fwd_tc_kernel<64>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-  });
+  static SmemLimit limit[2];  // <128>, <64>: set on each device's first launch
+  const cudaError_t attr_err = limit[d == 128 ? 0 : 1].ensure(kern, 227 * 1024);
   if (attr_err != cudaSuccess)
     return fail(IHA_ERR_CUDA, "premix forward (smem attribute): %s", cudaGetErrorString(attr_err));
   int grid = sm_count();
@@ -1031,13 +1024,8 @@ namespace {
 // per process (thread-safe) to the largest size any launch asks for.
 template <bool DX, bool DW>
 cudaError_t bwd_smem_attribute() {
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(premix_bwd_tc_kernel<DX, DW>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemMax);
-  });
-  return err;
+  static SmemLimit limit;  // per instantiation, set on each device's first launch
+  return limit.ensure(premix_bwd_tc_kernel<DX, DW>, kBwdSmemMax);
 }
 
 }  // namespace
