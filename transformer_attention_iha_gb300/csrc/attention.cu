@@ -57,6 +57,7 @@ constexpr int kStgBytes = 32 * 128;  // per softmax warp: 32 rows x 64 bf16 of O
 // Q 2x2, K 2x2, V 2x2 chunks | O staging of the 8 softmax warps
 constexpr int kSmemTiles = (4 + 2 * kKSlots + 4) * kTileChunkBytes + 8 * kStgBytes;
 constexpr int kSmemBytes = kSmemTiles + 512 + 1024;  // + barriers + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "attention forward: over the per-block shared memory limit");
 constexpr float kRescaleLog2 = 8.0f;
 // L2 budget for the K / V of one head group.
 constexpr int64_t kGroupKVBytes = 48ll << 20;
@@ -185,6 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* item_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  // 30 barriers, then the TMEM address, the abort flag and the 4-entry ring
+  static_assert(30 * 8 + 4 + 4 + 4 * 4 <= 512, "attention forward: barrier region");
   unsigned int* work = g_work[p.work_slot];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -64,6 +64,7 @@ constexpr int kCompute = 256;  // threads of warps 0-7
 constexpr int kSmemTiles = 7 * kTileB;
 constexpr int kLDBytes = 2 * 2 * kB * 4;  // 2 stages x (lse2, D) x 128 floats
 constexpr int kSmemBytes = kSmemTiles + kLDBytes + 512;
+static_assert(kSmemBytes <= 227 * 1024, "attention backward: over the per-block shared memory limit");
 
 struct BwdParams {
   int B, Hh, N, d, Npad, ksteps, nch;

@@ -58,6 +58,7 @@ constexpr int kTensorBytes = 2 * kChunkBytes;  // up to d = 128
 constexpr int kStageBytes = 3 * kTensorBytes;  // Q, K, V
 constexpr int kThreads = 320;
 constexpr int kSmemBytes = 2 * kStageBytes + 256 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "mask-unit attention: over the per-block shared memory limit");
 
 struct MuParams {
   int Bo, Bi, Hh, T, d, nch, ksteps, npv;
@@ -139,6 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto b_qpool = [&](int s) { return bar0 + 8u * (3 * NS + 10 + s); };  // Q of stage s pooled
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * NS + 10 + (FUSED ? 0 : NS));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // barriers, then the TMEM address and the abort flag, in the 256 bytes
+  static_assert(8 * (3 * NS + 10 + (FUSED ? 0 : NS)) + 4 + 4 <= 256,
+                "mask-unit attention: barrier region");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_my = (p.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
